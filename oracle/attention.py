@@ -1,0 +1,259 @@
+"""Plain CPU oracle for causal prefill attention with the ZYFA FP8 numerics.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path may import this module; only the tests,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` use it.  It shares no code,
+constant generator or helper with the CUDA library.
+
+What is computed, per batch b, head h and query row i (rows are independent, so any subset of rows
+may be evaluated; the row loop is chunked only to bound memory and does not change any arithmetic):
+
+* ``exact_causal_attention`` (O1): softmax(s_ij) over keys j <= i in float64 on the dequantised
+  FP8 inputs, with ``s_ij = scale * q_i . k_j``.  This is the definition of causal attention the
+  pages start from (ZYFA: Speed and Accuracy of FP8 FlashAttention on AMD CDNA4, abstract;
+  spbcomputers.ru ZYFA article, intro: causal forward attention for prefill).
+
+* ``leanp_causal_attention`` (O2): the three FP8 techniques, step by step, as the pages order them
+  (abstract techniques (1) and (3); spbcomputers.ru article, section "Три приёма"; captivela article,
+  section "Tiga Trik"):
+    1. raw score ``S32_ij = fl32(sum_d q8_id * k8_jd)`` over the e4m3 code values.  The sum of e4m3
+       products is exact in float64 for D <= 192, so this is the exact sum rounded once to fp32.
+    2. per-launch constant ``a = fl32(fl32(fl32(scale*dq)*dk) * fl32(8*log2 e))``; ``u = S32*a`` is the
+       score in units of 1/8 binade, i.e. in e4m3 code steps ("the code grows by 8 per doubling").
+    3. keys are grouped in blocks of 64, aligned at key 0; per (row, block) the exponent
+       ``e = ceil(max_j fl32(S32_ij*a) / 8)`` is the power of two that scales the block up so its
+       largest probability lands in (1/2, 1] before rounding (per-block power-of-two scaling).
+    4. Lean P: ``code = clamp(rne(fl32(S32*a + (c0 - 8e))), 0, 126)`` - one multiply-add and one
+       integer conversion instead of an exponential.  ``c0 = 55.625`` (reading; see below).
+    5. the weight a code stands for is ``dec_e4m3(code) * 2^(e - e_max)`` (the block scale is
+       removed inside the matrix product on the GPU; here it is an explicit power of two).
+    6. normalise by the sum of the rounded weights: ``O_i = dv * sum_j w_ij v8_j / sum_j w_ij``.
+
+  Reading of c0: the pages give only "8x + constant" and a per-probability error of at most 7.5%
+  against 5.9% for exact rounding.  ``rne(8x + c0)`` meets 7.5% over the normal range x in [-6, 0]
+  only for c0 in about [55.605, 55.65]; 55.625 = 445/8 is exact in fp32 and maps every integer x in
+  [-6, 0] to the exact code of 2^x, 8x + 56.  Blocks whose exponent lies more than 126 binades below
+  the row's largest block exponent get weight 0 (their scale leaves the e8m0 range).
+
+* ``plain_fp8_causal_attention`` (O3): the usual FP8 softmax, for comparison only: exact
+  probabilities relative to the row max, rounded to e4m3 once, divided by the unrounded sum.
+
+* ``bf16_causal_attention`` (O4): the BF16 twin.  ``x = fl32(S32*a')`` with ``a' = fl32(scale*log2 e)``,
+  integer reference ``M = ceil(max_j x_j)``, ``p_j = bf16(2^fl32(S32*a' - M))``, normalised by the sum
+  of the rounded ``p_j``.  The pages fix no BF16 numerics; this is the plainest reading that shares the
+  FP8 schedule (rounded-sum normalisation, no block scaling since bf16 has 8 exponent bits).
+
+Layouts follow flash_attn_func: q [B,S,H,Dqk], k [B,S,Hkv,Dqk], v [B,S,Hkv,Dv]; query head h reads
+KV head h // (H/Hkv).  Outputs are float64 [B, R, len(heads), Dv] for the requested rows R.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from .formats import e4m3_decode, e4m3_encode_rne_satfinite, fl32
+
+LEANP_C0 = 55.625
+SCALE_BLOCK = 64
+LOG2E = math.log2(math.e)
+LOG2E_F32 = float(np.float32(LOG2E))
+LOG2E_X8_F32 = float(np.float32(8.0 * LOG2E))
+_ROW_CHUNK = 256
+
+# Every positive finite bfloat16 value, ascending (the patterns 0x0000..0x7F7F are monotone).
+_BF16_POS = (np.arange(0, 0x7F80, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def default_softmax_scale(d_qk: int) -> float:
+    """flash_attn_func's default 1/sqrt(D_qk), rounded once to fp32."""
+    return float(np.float32(1.0 / math.sqrt(d_qk)))
+
+
+def fp8_score_scale(softmax_scale: float, dq: float, dk: float) -> float:
+    """a = fl32(fl32(fl32(scale*dq)*dk) * fl32(8 log2 e)), evaluated left to right in fp32."""
+    t = np.float32(np.float32(softmax_scale) * np.float32(dq))
+    t = np.float32(t * np.float32(dk))
+    return float(np.float32(t * np.float32(LOG2E_X8_F32)))
+
+
+def bf16_score_scale(softmax_scale: float) -> float:
+    """a' = fl32(scale * fl32(log2 e))."""
+    return float(np.float32(np.float32(softmax_scale) * np.float32(LOG2E_F32)))
+
+
+def bf16_round_f64(x) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 (ties to even pattern), one rounding."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    hi = np.clip(np.searchsorted(_BF16_POS, a, side="left"), 0, len(_BF16_POS) - 1)
+    lo = np.clip(hi - 1, 0, len(_BF16_POS) - 1)
+    dhi = _BF16_POS[hi] - a
+    dlo = a - _BF16_POS[lo]
+    pick = np.where((dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0)), hi, lo)
+    pick = np.where(_BF16_POS[hi] == a, hi, pick)
+    return np.copysign(_BF16_POS[pick], x)
+
+
+def leanp_code(u_plus_offset_exact) -> np.ndarray:
+    """Lean-P code from the exact value ``S32*a + (c0 - 8e)``: one fp32 rounding (as a fused
+    multiply-add produces), then round-half-to-even to an integer, clamped to [0, 126]."""
+    t = fl32(u_plus_offset_exact)
+    return np.clip(np.rint(t), 0, 126).astype(np.int64)
+
+
+def leanp_row_weights(s32, a: float, c0: float = LEANP_C0, block: int = SCALE_BLOCK):
+    """Lean-P weights for a set of rows whose keys are all visible (no mask).
+
+    ``s32``: [R, N] raw fp32 scores (as float64).  Returns (codes [R,N], e [R,nblocks], w [R,N]).
+    """
+    s32 = np.atleast_2d(np.asarray(s32, dtype=np.float64))
+    valid = np.ones(s32.shape, dtype=bool)
+    return _leanp_weights(s32, valid, a, c0, block)
+
+
+def _leanp_weights(s32, valid, a, c0, block):
+    r, n = s32.shape
+    nb = -(-n // block)
+    pad = nb * block - n
+    u = np.where(valid, fl32(s32 * a), -np.inf)
+    u_pad = np.pad(u, ((0, 0), (0, pad)), constant_values=-np.inf)
+    u_max = u_pad.reshape(r, nb, block).max(axis=2)                      # [R, nb], -inf if empty
+    with np.errstate(invalid="ignore"):
+        e = np.ceil(u_max * 0.125)
+    e_key = np.repeat(e, block, axis=1)[:, :n]
+    e_safe = np.where(np.isfinite(e_key), e_key, 0.0)
+    code = leanp_code(s32 * a + (c0 - 8.0 * e_safe))
+    code = np.where(valid, code, 0)
+    e_max = np.max(np.where(np.isfinite(e), e, -np.inf), axis=1, keepdims=True)
+    rel = e_safe - e_max
+    w = e4m3_decode(code.astype(np.uint8)) * np.exp2(np.where(valid, rel, 0.0))
+    w = np.where(valid & (rel >= -126), w, 0.0)
+    return code, e, w
+
+
+def _heads(h_total, heads):
+    return list(range(h_total)) if heads is None else list(heads)
+
+
+def _rows(s, rows):
+    return np.arange(s) if rows is None else np.asarray(rows, dtype=np.int64)
+
+
+def _causal_mask(row_idx, n_keys):
+    return np.arange(n_keys)[None, :] <= row_idx[:, None]
+
+
+def exact_causal_attention(q, k, v, softmax_scale, rows=None, heads=None) -> np.ndarray:
+    """O1: float64 causal attention on real-valued (dequantised) inputs."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    b_, s_, h_, _ = q.shape
+    hkv, dv = k.shape[2], v.shape[3]
+    rows = _rows(s_, rows)
+    hs = _heads(h_, heads)
+    out = np.zeros((b_, len(rows), len(hs), dv))
+    for b in range(b_):
+        for oi, h in enumerate(hs):
+            kh = h // (h_ // hkv)
+            kk, vv = k[b, :, kh, :], v[b, :, kh, :]
+            for c in range(0, len(rows), _ROW_CHUNK):
+                ri = rows[c:c + _ROW_CHUNK]
+                n = int(ri.max()) + 1 if len(ri) else 0
+                s = softmax_scale * (q[b, ri, h, :] @ kk[:n].T)
+                mask = _causal_mask(ri, n)
+                s = np.where(mask, s, -np.inf)
+                p = np.exp(s - s.max(axis=1, keepdims=True))
+                out[b, c:c + len(ri), oi, :] = (p @ vv[:n]) / p.sum(axis=1, keepdims=True)
+    return out
+
+
+def dequant_e4m3(x8, descale: float) -> np.ndarray:
+    """deq(x8) * descale: the real values an FP8 tensor with a per-tensor descale stands for."""
+    return e4m3_decode(x8) * float(descale)
+
+
+def leanp_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=None, heads=None,
+                           c0: float = LEANP_C0, return_codes: bool = False):
+    """O2: Lean P + per-64-key power-of-two block scaling + rounded-row-sum normalisation."""
+    qd, kd, vd = e4m3_decode(q8), e4m3_decode(k8), e4m3_decode(v8)
+    a = fp8_score_scale(softmax_scale, dq, dk)
+    b_, s_, h_, _ = qd.shape
+    hkv, dvd = kd.shape[2], vd.shape[3]
+    rows = _rows(s_, rows)
+    hs = _heads(h_, heads)
+    out = np.zeros((b_, len(rows), len(hs), dvd))
+    codes_out = {}
+    for b in range(b_):
+        for oi, h in enumerate(hs):
+            kh = h // (h_ // hkv)
+            kk, vv = kd[b, :, kh, :], vd[b, :, kh, :]
+            for c in range(0, len(rows), _ROW_CHUNK):
+                ri = rows[c:c + _ROW_CHUNK]
+                n = int(ri.max()) + 1 if len(ri) else 0
+                s32 = fl32(qd[b, ri, h, :] @ kk[:n].T)
+                code, _, w = _leanp_weights(s32, _causal_mask(ri, n), a, c0, SCALE_BLOCK)
+                out[b, c:c + len(ri), oi, :] = float(dv) * (w @ vv[:n]) / w.sum(axis=1, keepdims=True)
+                if return_codes:
+                    codes_out[(b, h, c)] = code
+    return (out, codes_out) if return_codes else out
+
+
+def plain_fp8_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=None, heads=None):
+    """O3: exact probabilities relative to the row max, rounded once to e4m3, unrounded sum."""
+    qd, kd, vd = e4m3_decode(q8), e4m3_decode(k8), e4m3_decode(v8)
+    a = fp8_score_scale(softmax_scale, dq, dk)
+    b_, s_, h_, _ = qd.shape
+    hkv, dvd = kd.shape[2], vd.shape[3]
+    rows = _rows(s_, rows)
+    hs = _heads(h_, heads)
+    out = np.zeros((b_, len(rows), len(hs), dvd))
+    for b in range(b_):
+        for oi, h in enumerate(hs):
+            kh = h // (h_ // hkv)
+            kk, vv = kd[b, :, kh, :], vd[b, :, kh, :]
+            for c in range(0, len(rows), _ROW_CHUNK):
+                ri = rows[c:c + _ROW_CHUNK]
+                n = int(ri.max()) + 1 if len(ri) else 0
+                y = fl32(qd[b, ri, h, :] @ kk[:n].T) * a / 8.0
+                y = np.where(_causal_mask(ri, n), y, -np.inf)
+                p = np.exp2(y - y.max(axis=1, keepdims=True))
+                p8 = e4m3_decode(e4m3_encode_rne_satfinite(p))
+                out[b, c:c + len(ri), oi, :] = float(dv) * (p8 @ vv[:n]) / p.sum(axis=1, keepdims=True)
+    return out
+
+
+def bf16_causal_attention(qb, kb, vb, softmax_scale, rows=None, heads=None):
+    """O4: the BF16 twin on bf16-valued inputs (float64 arrays holding bf16 values)."""
+    qb = np.asarray(qb, dtype=np.float64)
+    kb = np.asarray(kb, dtype=np.float64)
+    vb = np.asarray(vb, dtype=np.float64)
+    a2 = bf16_score_scale(softmax_scale)
+    b_, s_, h_, _ = qb.shape
+    hkv, dvd = kb.shape[2], vb.shape[3]
+    rows = _rows(s_, rows)
+    hs = _heads(h_, heads)
+    out = np.zeros((b_, len(rows), len(hs), dvd))
+    for b in range(b_):
+        for oi, h in enumerate(hs):
+            kh = h // (h_ // hkv)
+            kk, vv = kb[b, :, kh, :], vb[b, :, kh, :]
+            for c in range(0, len(rows), _ROW_CHUNK):
+                ri = rows[c:c + _ROW_CHUNK]
+                n = int(ri.max()) + 1 if len(ri) else 0
+                s32 = fl32(qb[b, ri, h, :] @ kk[:n].T)
+                mask = _causal_mask(ri, n)
+                x = np.where(mask, fl32(s32 * a2), -np.inf)
+                m = np.ceil(x.max(axis=1, keepdims=True))
+                t = fl32(s32 * a2 - m)
+                p = np.where(mask, bf16_round_f64(np.exp2(np.where(mask, t, 0.0))), 0.0)
+                out[b, c:c + len(ri), oi, :] = (p @ vv[:n]) / p.sum(axis=1, keepdims=True)
+    return out
+
+
+def rel_l2(x, ref) -> float:
+    """||x - ref||_2 / ||ref||_2 over all elements."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = float(np.linalg.norm(ref.ravel()))
+    return float(np.linalg.norm((x - ref).ravel())) / (den if den > 0 else 1.0)
