@@ -1,0 +1,124 @@
+"""Thin Python binding of libzyfa.so (argument marshalling only; every step runs in the CUDA library).
+
+``zyfa_attn_fwd_causal`` mirrors the C entry point (raw device addresses and sizes);
+``flash_attn_func`` is the tensor-level call in the flash_attn_func style the pages describe
+(spbcomputers.ru ZYFA article, intro: a drop-in flash_attn_func-compatible interface).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libzyfa.so")
+_lib = None
+_lock = threading.Lock()
+
+ZYFA_DTYPE_E4M3 = 0
+ZYFA_DTYPE_BF16 = 1
+STATUS = {0: "ZYFA_OK", 1: "ZYFA_ERR_INVALID_ARG", 2: "ZYFA_ERR_UNSUPPORTED", 3: "ZYFA_ERR_MISALIGNED",
+          4: "ZYFA_ERR_CUDA", 5: "ZYFA_ERR_TIMEOUT"}
+EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_check_errors", "zyfa_status_string", "zyfa_kernel_launches")
+
+
+class ZyfaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libzyfa.so; raises if it has not been built (there is no fallback path)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise ZyfaError(4, f"{_LIB_PATH} is missing; build it with `python -m fp8_causal_prefill_gb300.build`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.zyfa_attn_fwd_causal.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, vp, vp, vp]
+        lib.zyfa_attn_fwd_causal.restype = ci
+        lib.zyfa_check_errors.argtypes = [vp]
+        lib.zyfa_check_errors.restype = ci
+        lib.zyfa_status_string.argtypes = [ci]
+        lib.zyfa_status_string.restype = ctypes.c_char_p
+        lib.zyfa_kernel_launches.argtypes = [ci, ci, ci]
+        lib.zyfa_kernel_launches.restype = ci
+        _lib = lib
+        return lib
+
+
+def zyfa_attn_fwd_causal(q: int, k: int, v: int, out: int, B: int, S: int, H: int, H_kv: int, D_qk: int, D_v: int,
+                         softmax_scale: float, dtype: int, q_descale: int = 0, k_descale: int = 0,
+                         v_descale: int = 0, stream: int = 0) -> int:
+    """Call the C entry point with raw addresses; returns the status code."""
+    lib = load_library()
+    return lib.zyfa_attn_fwd_causal(q, k, v, out, B, S, H, H_kv, D_qk, D_v, float(softmax_scale), dtype,
+                                    q_descale or None, k_descale or None, v_descale or None, stream or None)
+
+
+def zyfa_check_errors(stream: int = 0) -> int:
+    return load_library().zyfa_check_errors(stream or None)
+
+
+def zyfa_kernel_launches(B: int, S: int, H: int) -> int:
+    return load_library().zyfa_kernel_launches(B, S, H)
+
+
+def _ptr_or_zero(t):
+    if t is None:
+        return 0
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32 and t.numel() == 1):
+        raise TypeError("descale must be a 1-element float32 CUDA tensor or None")
+    return t.data_ptr()
+
+
+def flash_attn_func(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: float | None = None,
+                    causal: bool = True, q_descale=None, k_descale=None, v_descale=None,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+    """Causal prefill attention on CUDA tensors q [B,S,H,D_qk], k [B,S,H_kv,D_qk], v [B,S,H_kv,D_v].
+
+    FP8 inputs are ``torch.float8_e4m3fn`` (or ``torch.uint8`` holding e4m3 bit patterns) with optional
+    per-tensor descales (1-element float32 CUDA tensors); BF16 inputs are ``torch.bfloat16``.  Returns a
+    bfloat16 tensor [B,S,H,D_v].  Runs on the current CUDA stream.
+    """
+    if not causal:
+        raise NotImplementedError("only causal attention is implemented")
+    if q.dtype in (torch.float8_e4m3fn, torch.uint8):
+        dtype = ZYFA_DTYPE_E4M3
+    elif q.dtype == torch.bfloat16:
+        dtype = ZYFA_DTYPE_BF16
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, S, heads, D]")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    B, S, H, D_qk = q.shape
+    _, _, H_kv, D_v = v.shape
+    if k.shape != (B, S, H_kv, D_qk) or v.shape[:2] != (B, S):
+        raise ValueError("inconsistent q/k/v shapes")
+    if out is None:
+        out = torch.empty((B, S, H, D_v), dtype=torch.bfloat16, device=q.device)
+    elif out.shape != (B, S, H, D_v) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bfloat16 [B,S,H,D_v] tensor")
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = zyfa_attn_fwd_causal(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, H, H_kv, D_qk,
+                                  D_v, 0.0 if softmax_scale is None else softmax_scale, dtype,
+                                  _ptr_or_zero(q_descale), _ptr_or_zero(k_descale), _ptr_or_zero(v_descale),
+                                  stream)
+    if st != 0:
+        raise ZyfaError(st, "zyfa_attn_fwd_causal")
+    return out

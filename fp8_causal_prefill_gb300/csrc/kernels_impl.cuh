@@ -1,0 +1,40 @@
+// Launch wrapper shared by the FP8 and BF16 kernel translation units.
+#pragma once
+#include "launch.h"
+#include "zyfa_fwd.cuh"
+
+namespace zyfa {
+
+template <bool FP8, int DQK, int DV>
+int smem_bytes() {
+  return Cfg<FP8, DQK, DV>::kSmemBytes;
+}
+
+template <bool FP8, int DQK, int DV>
+cudaError_t launch_fwd(const LaunchArgs& a) {
+  using C = Cfg<FP8, DQK, DV>;
+  auto kernel = zyfa_fwd_kernel<FP8, DQK, DV>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  Params p;
+  p.q = static_cast<const uint8_t*>(a.q);
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.q_descale = a.q_descale;
+  p.k_descale = a.k_descale;
+  p.v_descale = a.v_descale;
+  p.B = a.B;
+  p.S = a.S;
+  p.H = a.H;
+  p.H_kv = a.H_kv;
+  p.softmax_scale = a.softmax_scale;
+  p.num_units = a.num_units;
+  p.status = a.status;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = a.stream;
+  return cudaLaunchKernelEx(&cfg, kernel, p, a.tm_q, a.tm_k0, a.tm_k1, a.tm_v);
+}
+
+}  // namespace zyfa

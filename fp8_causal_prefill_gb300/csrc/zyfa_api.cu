@@ -1,0 +1,175 @@
+// C ABI of libzyfa.so: argument checks, TMA tensor maps, per-device status word, dispatch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/zyfa.h"
+#include "launch.h"
+
+namespace {
+
+// Set by a kernel that gave up on a pipeline wait; read and cleared by zyfa_check_errors.
+__device__ int g_zyfa_status;
+
+constexpr int kMaxDevices = 64;
+constexpr int kUnitRows = 256;  // query rows per work unit (two 128-row tiles)
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int*> g_status_ptr[kMaxDevices];
+
+// Device-side address of the status word for the current device (looked up once per device).
+int* status_ptr(int dev) {
+  int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_zyfa_status) != cudaSuccess) return nullptr;
+  g_status_ptr[dev].store(static_cast<int*>(addr), std::memory_order_release);
+  return static_cast<int*>(addr);
+}
+
+int sm_count(int dev) {
+  int n = g_sm_count[dev].load(std::memory_order_acquire);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+  g_sm_count[dev].store(n, std::memory_order_release);
+  return n;
+}
+
+// 4-D map over a [B][S][heads][D] tensor: box = {box_inner elements of D, 1 head, box_rows rows, 1}.
+bool make_map(CUtensorMap* m, const void* base, bool fp8, int D, int heads, int S, int B, int box_inner,
+              int box_rows, CUtensorMapSwizzle sw) {
+  const int es = fp8 ? 1 : 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * es, static_cast<cuuint64_t>(heads) * D * es,
+                           static_cast<cuuint64_t>(S) * heads * D * es};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool FP8, int DQK, int DV>
+zyfa_status_t run(zyfa::LaunchArgs& a, const void* q, const void* k, const void* v) {
+  constexpr int es = FP8 ? 1 : 2;
+  constexpr int kRowK = DQK * es, kRowV = DV * es;
+  constexpr int kChunk = 128 / es;  // elements per 128-byte chunk
+  bool ok = true;
+  // K: 128-byte chunks with the 128-byte swizzle, plus a 64-byte tail chunk with the 64-byte swizzle
+  if (kRowK >= 128) ok &= make_map(&a.tm_k0, k, FP8, DQK, a.H_kv, a.S, a.B, kChunk, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (kRowK % 128 == 64) ok &= make_map(&a.tm_k1, k, FP8, DQK, a.H_kv, a.S, a.B, 64 / es, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (kRowK < 128) a.tm_k0 = a.tm_k1;
+  if (kRowK % 128 != 64) a.tm_k1 = a.tm_k0;
+  // V: MN-major tiles, one swizzle atom per 128 bytes of the value row
+  ok &= make_map(&a.tm_v, v, FP8, DV, a.H_kv, a.S, a.B, kRowV >= 128 ? kChunk : DV, 64,
+                 kRowV >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!FP8) ok &= make_map(&a.tm_q, q, FP8, DQK, a.H, a.S, a.B, kChunk, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  else a.tm_q = a.tm_v;
+  if (!ok) return ZYFA_ERR_CUDA;
+  return zyfa::launch_fwd<FP8, DQK, DV>(a) == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* zyfa_status_string(zyfa_status_t s) {
+  switch (s) {
+    case ZYFA_OK: return "ZYFA_OK";
+    case ZYFA_ERR_INVALID_ARG: return "ZYFA_ERR_INVALID_ARG";
+    case ZYFA_ERR_UNSUPPORTED: return "ZYFA_ERR_UNSUPPORTED";
+    case ZYFA_ERR_MISALIGNED: return "ZYFA_ERR_MISALIGNED";
+    case ZYFA_ERR_CUDA: return "ZYFA_ERR_CUDA";
+    case ZYFA_ERR_TIMEOUT: return "ZYFA_ERR_TIMEOUT";
+  }
+  return "ZYFA_ERR_UNKNOWN";
+}
+
+int zyfa_kernel_launches(int B, int S, int H) { return (B > 0 && S > 0 && H > 0) ? 1 : 0; }
+
+zyfa_status_t zyfa_attn_fwd_causal(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
+                                   int H_kv, int D_qk, int D_v, float softmax_scale, zyfa_dtype_t dtype,
+                                   const float* q_descale, const float* k_descale, const float* v_descale,
+                                   cudaStream_t stream) {
+  if (B < 1 || H < 1 || H_kv < 1 || S < 0 || H % H_kv != 0) return ZYFA_ERR_INVALID_ARG;
+  if (dtype != ZYFA_DTYPE_E4M3 && dtype != ZYFA_DTYPE_BF16) return ZYFA_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale) || softmax_scale < 0.0f) return ZYFA_ERR_INVALID_ARG;
+  const bool shape_ok = (D_qk == 64 && D_v == 64) || (D_qk == 128 && D_v == 128) || (D_qk == 192 && D_v == 128);
+  if (!shape_ok) return ZYFA_ERR_UNSUPPORTED;
+  if (S == 0) return ZYFA_OK;
+  if (!q || !k || !v || !out) return ZYFA_ERR_INVALID_ARG;
+  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out)) return ZYFA_ERR_MISALIGNED;
+  const long long nqb = (static_cast<long long>(S) + kUnitRows - 1) / kUnitRows;
+  const long long units = nqb * B * H;
+  if (units > (1ll << 30) || static_cast<long long>(S) > (1ll << 30)) return ZYFA_ERR_UNSUPPORTED;
+  if (softmax_scale == 0.0f) softmax_scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D_qk)));
+  if (!get_encode()) return ZYFA_ERR_CUDA;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ZYFA_ERR_CUDA;
+  const int nsm = sm_count(dev);
+  int* status = status_ptr(dev);
+  if (nsm <= 0 || !status) return ZYFA_ERR_CUDA;
+
+  zyfa::LaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.out = out;
+  const bool fp8 = dtype == ZYFA_DTYPE_E4M3;
+  a.q_descale = fp8 ? q_descale : nullptr;
+  a.k_descale = fp8 ? k_descale : nullptr;
+  a.v_descale = fp8 ? v_descale : nullptr;
+  a.B = B;
+  a.S = S;
+  a.H = H;
+  a.H_kv = H_kv;
+  a.softmax_scale = softmax_scale;
+  a.num_units = static_cast<int>(units);
+  a.status = status;
+  a.grid = static_cast<int>(units < nsm ? units : nsm);
+  a.stream = stream;
+  if (fp8) {
+    if (D_qk == 64) return run<true, 64, 64>(a, q, k, v);
+    if (D_qk == 128) return run<true, 128, 128>(a, q, k, v);
+    return run<true, 192, 128>(a, q, k, v);
+  }
+  if (D_qk == 64) return run<false, 64, 64>(a, q, k, v);
+  if (D_qk == 128) return run<false, 128, 128>(a, q, k, v);
+  return run<false, 192, 128>(a, q, k, v);
+}
+
+zyfa_status_t zyfa_check_errors(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ZYFA_ERR_CUDA;
+  int value = 0;
+  if (cudaMemcpyFromSymbol(&value, g_zyfa_status, sizeof(int)) != cudaSuccess) return ZYFA_ERR_CUDA;
+  if (value != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_zyfa_status, &zero, sizeof(int)) != cudaSuccess) return ZYFA_ERR_CUDA;
+    return ZYFA_ERR_TIMEOUT;
+  }
+  return ZYFA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,11 @@
+// BF16 instantiations of the causal prefill kernel (same schedule as FP8).
+#include "kernels_impl.cuh"
+
+namespace zyfa {
+template cudaError_t launch_fwd<false, 64, 64>(const LaunchArgs&);
+template cudaError_t launch_fwd<false, 128, 128>(const LaunchArgs&);
+template cudaError_t launch_fwd<false, 192, 128>(const LaunchArgs&);
+template int smem_bytes<false, 64, 64>();
+template int smem_bytes<false, 128, 128>();
+template int smem_bytes<false, 192, 128>();
+}  // namespace zyfa

@@ -1,0 +1,97 @@
+/*
+ * zyfa.h - C ABI of the GB300 (sm_103a) causal prefill attention library (libzyfa.so).
+ *
+ * The operation (ZYFA: Speed and Accuracy of FP8 FlashAttention on AMD CDNA4, abstract; spbcomputers.ru
+ * ZYFA article, intro and FAQ "Это готовый сервер инференса?": a flash_attn_func-compatible kernel
+ * library for causal forward attention in the prefill phase, FP8 e4m3 and BF16):
+ *
+ *     out[b, i, h, :] = sum_{j <= i} softmax_j(scale * q[b,i,h,:] . k[b,j,hk,:]) * v[b,j,hk,:]
+ *     hk = h / (H / H_kv)   (grouped-query attention; H_kv == H is plain multi-head attention)
+ *
+ * FP8 numerics (same sources, abstract techniques (1) and (3); spbcomputers.ru article, section
+ * "Три приёма"): probabilities are produced directly as e4m3 codes by one multiply-add and one
+ * rounding ("Lean P": code(2^x) = rne(8x + 55.625)); every (row, 64-key block) of probabilities is
+ * scaled up by a power of two before rounding and the scale is removed inside the PV product; the
+ * output is normalised by the sum of the already-rounded probabilities.  BF16 numerics: probabilities
+ * 2^(x - M) rounded to bf16, normalised by the sum of the rounded values.
+ *
+ * Memory layout (all tensors dense, row-major, flash_attn_func order, device memory):
+ *     q   [B, S, H,    D_qk]   e4m3 (one byte per element) or bf16
+ *     k   [B, S, H_kv, D_qk]   same type as q
+ *     v   [B, S, H_kv, D_v ]   same type as q
+ *     out [B, S, H,    D_v ]   bf16, written in full for every call with S > 0
+ * Supported head shapes (D_qk, D_v): (64, 64), (128, 128), (192, 128) (the last one is the
+ * DeepSeek-style multi-head latent attention shape, 128 "nope" + 64 rotary dims).
+ */
+#ifndef ZYFA_H_
+#define ZYFA_H_
+
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ZYFA_DTYPE_E4M3 = 0, /* OCP FP8 e4m3 ("fn"): q, k, v hold bit patterns, one byte each */
+  ZYFA_DTYPE_BF16 = 1
+} zyfa_dtype_t;
+
+typedef enum {
+  ZYFA_OK = 0,
+  ZYFA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, H % H_kv != 0, bad scale, bad dtype */
+  ZYFA_ERR_UNSUPPORTED = 2, /* head shape outside the supported list, or sizes beyond int range   */
+  ZYFA_ERR_MISALIGNED = 3,  /* q, k, v or out not 16-byte aligned (TMA and vector stores need it) */
+  ZYFA_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed (launch, attribute, tensor map) */
+  ZYFA_ERR_TIMEOUT = 5      /* a kernel gave up waiting on a pipeline barrier (see check_errors)  */
+} zyfa_status_t;
+
+/*
+ * zyfa_attn_fwd_causal - causal forward attention, asynchronous on `stream`.
+ *
+ *   q, k, v, out   device pointers in the layout above; the caller owns them.  out must not alias
+ *                  q, k or v.
+ *   B, S, H, H_kv  batch, sequence length (queries and keys), query heads, key/value heads;
+ *                  B, H, H_kv >= 1, S >= 0, H % H_kv == 0.  S == 0 returns ZYFA_OK with no launch.
+ *   D_qk, D_v      head dims of q/k and of v/out, one of the supported pairs.
+ *   softmax_scale  multiplier of q.k; 0 selects the flash_attn_func default (float)(1/sqrt(D_qk)).
+ *                  Negative, NaN or infinite values are rejected.
+ *   dtype          ZYFA_DTYPE_E4M3 or ZYFA_DTYPE_BF16 (type of q, k, v).
+ *   q_descale, k_descale, v_descale
+ *                  FP8 only: device pointers to one fp32 each, the per-tensor factor that turns a
+ *                  stored e4m3 value into the real value (real = e4m3 * descale).  NULL means 1.0.
+ *                  Ignored for BF16.  Read on the device, so no host synchronisation happens.
+ *   stream         CUDA stream (0 = legacy default stream).
+ *
+ * Returns ZYFA_OK once the kernel is enqueued; argument errors are returned before anything is
+ * enqueued.  The call allocates no memory, keeps no per-call state and may be issued concurrently
+ * from several host threads.  Results are bitwise reproducible for identical inputs.  A kernel that
+ * stops on a pipeline timeout records ZYFA_ERR_TIMEOUT in a per-device status word that
+ * zyfa_check_errors() reports; the output of that launch is then unspecified.
+ */
+zyfa_status_t zyfa_attn_fwd_causal(const void* q, const void* k, const void* v, void* out, int B, int S,
+                                   int H, int H_kv, int D_qk, int D_v, float softmax_scale,
+                                   zyfa_dtype_t dtype, const float* q_descale, const float* k_descale,
+                                   const float* v_descale, cudaStream_t stream);
+
+/*
+ * zyfa_check_errors - synchronise `stream`, then read and clear the current device's status word.
+ * Returns ZYFA_ERR_TIMEOUT if any kernel of this library timed out since the last check,
+ * ZYFA_ERR_CUDA if the synchronisation itself failed, ZYFA_OK otherwise.
+ */
+zyfa_status_t zyfa_check_errors(cudaStream_t stream);
+
+/* zyfa_status_string - static, human-readable name of a status code (never NULL). */
+const char* zyfa_status_string(zyfa_status_t status);
+
+/*
+ * zyfa_kernel_launches - number of kernel launches one zyfa_attn_fwd_causal call with these sizes
+ * enqueues (0 for S == 0, else 1).  Pure host arithmetic, for accounting in benchmarks.
+ */
+int zyfa_kernel_launches(int B, int S, int H);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZYFA_H_ */
