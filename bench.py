@@ -1,0 +1,340 @@
+"""Benchmark: causal FP8 prefill attention TFLOP/s at S=32K, D=128 (and % of the GB300 FP8 peak).
+
+One step = one zyfa_attn_fwd_causal call over the whole workload B=1, H=32, H_kv=8, S=32768, D=128
+(Gaussian inputs quantised to e4m3 with per-tensor descales).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--dtype fp8|bf16] [--config bench32k|mla32k|...]
+  python bench.py --impl reference ...     # the CPU oracle on the host cores, same metric and workload
+
+FLOP convention: ``value`` counts the algorithmic causal FLOPs B*H*S^2*(D_qk+D_v) (half the dense count,
+what the tensor cores must execute); ``value_dense_formula`` reports the 2*B*H*S^2*(D_qk+D_v) variant.
+Under torchrun (N > 1) every rank runs its own replica of the workload (no data exchange); ``value``
+is the sum over ranks of the FLOPs divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal FP8 prefill attention TFLOP/s at S=32K D=128 and % of GB300 FP8 peak"
+# Nominal dense tensor peaks (PFLOP/s) used only for the FP8:BF16 ratio applied to the measured bf16 peak.
+NOMINAL_RATIO_FP8_TO_BF16 = 4.5 / 2.25
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["zyfa", "reference"], default="zyfa")
+    ap.add_argument("--dtype", choices=["fp8", "bf16"], default="fp8")
+    ap.add_argument("--config", default="bench32k")
+    ap.add_argument("--heads", type=int, default=0, help="override H (profiling a smaller case)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def shape_for(args):
+    from fp8_causal_prefill_gb300.inputs import CONFIGS, Shape
+    sh = CONFIGS[args.config]
+    if args.heads:
+        hkv = max(1, args.heads * sh.H_kv // sh.H)
+        sh = Shape(sh.B, sh.S, args.heads, hkv, sh.D_qk, sh.D_v, sh.kind)
+    return sh
+
+
+def workload_name(sh, dtype):
+    return (f"{'e4m3' if dtype == 'fp8' else 'bf16'} causal prefill B={sh.B} H={sh.H} H_kv={sh.H_kv} S={sh.S} "
+            f"D_qk={sh.D_qk} D_v={sh.D_v} {sh.kind} inputs")
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="zyfa_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_median": statistics.median(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def cpu_oracle_sample(p, dtype, budget_s):
+    """Time the oracle on a seeded sample of query rows of the workload (rows are independent)."""
+    import numpy as np
+
+    import oracle as O
+
+    sh = p.shape
+    sc = O.default_softmax_scale(sh.D_qk)
+    rng = np.random.default_rng(123)
+    done_rows, flops, elapsed, calls = 0, 0.0, 0.0, 0
+    while elapsed < budget_s and calls < 64:
+        rows = np.sort(rng.choice(sh.S, size=min(sh.S, 256), replace=False))
+        head = int(rng.integers(0, sh.H))
+        t0 = time.perf_counter()
+        if dtype == "fp8":
+            O.leanp_causal_attention(p.q8.numpy(), p.k8.numpy(), p.v8.numpy(), p.dq, p.dk, p.dv, sc, rows=rows,
+                                     heads=[head])
+        else:
+            f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+            O.bf16_causal_attention(f(p.qb), f(p.kb), f(p.vb), sc, rows=rows, heads=[head])
+        elapsed += time.perf_counter() - t0
+        flops += float(np.sum(2.0 * (rows + 1) * (sh.D_qk + sh.D_v))) * sh.B
+        done_rows += len(rows)
+        calls += 1
+    return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{done_rows} query rows x 1 head of {workload_name(sh, dtype)} "
+                      f"(seeded uniform rows, {flops:.3e} causal FLOPs in {elapsed:.1f} s; numpy float64, "
+                      f"BLAS threads = cores)"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is a bounded row sample of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from fp8_causal_prefill_gb300.inputs import make_problem
+
+    sh = shape_for(args)
+    p = make_problem(sh, seed=0, bf16=(args.dtype == "bf16"), fp8=(args.dtype == "fp8"))
+    per_step = max(0.5, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(p, args.dtype, per_step / 4)
+    vals = [cpu_oracle_sample(p, args.dtype, per_step) for _ in range(args.steps)]
+    value = statistics.median(v["value"] for v in vals)
+    cpu = dict(vals[-1])
+    cpu["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(sh, args.dtype), "sample": cpu["sample"]},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    from fp8_causal_prefill_gb300 import api
+    from fp8_causal_prefill_gb300.inputs import make_problem
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    sh = shape_for(args)
+    p = make_problem(sh, seed=rank, bf16=(args.dtype == "bf16"), fp8=(args.dtype == "fp8"))
+    if args.dtype == "fp8":
+        host = [t.contiguous() for t in (p.q8, p.k8, p.v8)]
+        dtype_code = api.ZYFA_DTYPE_E4M3
+    else:
+        host = [t.contiguous() for t in (p.qb, p.kb, p.vb)]
+        dtype_code = api.ZYFA_DTYPE_BF16
+    dq, dk, dv = (t.to(dev) for t in host)
+    desc = torch.tensor([p.dq, p.dk, p.dv], dtype=torch.float32, device=dev)
+    out = torch.empty((sh.B, sh.S, sh.H, sh.D_v), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    api.load_library()
+
+    def step(q, k, v, o):
+        st = api.zyfa_attn_fwd_causal(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), sh.B, sh.S, sh.H,
+                                      sh.H_kv, sh.D_qk, sh.D_v, 0.0, dtype_code,
+                                      desc.data_ptr() if args.dtype == "fp8" else 0,
+                                      desc.data_ptr() + 4 if args.dtype == "fp8" else 0,
+                                      desc.data_ptr() + 8 if args.dtype == "fp8" else 0, sptr)
+        if st != 0:
+            raise api.ZyfaError(st, "zyfa_attn_fwd_causal")
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+
+    flops = sh.causal_flops                      # per step per rank
+    for _ in range(max(3, args.warmup)):
+        step(dq, dk, dv, out)
+    barrier()
+
+    smi_index = local
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    if local < len(visible) and visible[local].strip().isdigit():
+        smi_index = int(visible[local])
+    sampler = ClockSampler(smi_index)
+    if rank == 0:
+        sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(dq, dk, dv, out)
+        ends[i].record(stream)
+    barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    total_ms = starts[0].elapsed_time(ends[-1])
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_per_step = float(t.item()) / args.steps
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    zst = api.zyfa_check_errors(sptr)
+    if zst != 0:
+        raise api.ZyfaError(zst, "kernel status")
+
+    # end to end through the same C entry point with host buffers: H2D of q/k/v, the call, D2H of out
+    e2e = None
+    if not args.no_e2e:
+        hpin = [h.pin_memory() for h in host]
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(h.numel() * h.element_size() for h in hpin) + (12 if args.dtype == "fp8" else 0)
+        hdesc = torch.tensor([p.dq, p.dk, p.dv], dtype=torch.float32).pin_memory()
+        d2h = hout.numel() * hout.element_size()
+        n_e2e = max(3, min(args.steps, 20))
+        for _ in range(2):
+            for h, d in zip(hpin, (dq, dk, dv)):
+                d.copy_(h, non_blocking=True)
+            step(dq, dk, dv, out)
+            hout.copy_(out, non_blocking=True)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            for h, d in zip(hpin, (dq, dk, dv)):
+                d.copy_(h, non_blocking=True)
+            if args.dtype == "fp8":
+                desc.copy_(hdesc, non_blocking=True)
+            step(dq, dk, dv, out)
+            hout.copy_(out, non_blocking=True)
+        e1.record(stream)
+        barrier()
+        te = torch.tensor([e0.elapsed_time(e1) / n_e2e], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": flops * world / (float(te.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": float(te.item()),
+               "steps": n_e2e}
+
+    if rank == 0:
+        peaks, src = load_peaks()
+        is_fp8 = args.dtype == "fp8"
+        ratio = NOMINAL_RATIO_FP8_TO_BF16 if is_fp8 else 1.0
+        peak = peaks["bf16_tflops"] * ratio
+        peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * ratio
+        avg_kernel_ms = statistics.fmean(kernel_ms)
+        achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
+        traffic = None
+        tpath = os.path.join(ROOT, "profiles", "dram_traffic.json")
+        if os.path.exists(tpath):
+            with open(tpath) as f:
+                td = json.load(f)
+            key = f"{args.dtype}:{args.config}"
+            if key in td and not args.heads:
+                traffic = td[key].get("bytes_per_launch")
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3" if is_fp8 else "bf16", "data": "synthetic",
+            "config": {"workload": workload_name(sh, args.dtype), "l2": "inputs 192 MB + output 256 MB per step "
+                       "exceed the 129 MB L2; no flush" if sh.S >= 16384 else "working set may fit in L2",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "value_dense_formula": 2.0 * value,
+            "pct_of_fp8_peak": 100.0 * value / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": (f"{src}: bf16 burst {peaks['bf16_tflops']} TFLOP/s x {ratio:g} "
+                                         f"(nominal {'fp8' if is_fp8 else 'bf16'}/bf16 ratio)"),
+                         "frac_of_sustained": achieved / peak_sus},
+            "kernel_ms": {"mean": avg_kernel_ms, "min": min(kernel_ms), "max": max(kernel_ms)},
+            "gpu_launches": args.steps * api.zyfa_kernel_launches(sh.B, sh.S, sh.H),
+            "clocks": clocks,
+        }
+        if e2e is not None:
+            line["e2e"] = e2e
+        if not args.no_cpu and world >= 1:
+            line["cpu_baseline"] = cpu_oracle_sample(p, args.dtype, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
