@@ -6,6 +6,7 @@ The three translation units compile in parallel; the shared library lands next t
 from __future__ import annotations
 
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -17,6 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzyfa.so")
 SOURCES = ["zyfa_api.cu", "zyfa_kernels_fp8.cu", "zyfa_kernels_bf16.cu"]
+# The attention kernel splits its registers between warpgroups at run time (setmaxnreg); the split is
+# sized for exactly this many registers per thread at launch, which every instantiation must get.
+KERNEL_REGS = 168
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + os.path.join(ROOT, "include")]
 
@@ -26,6 +30,26 @@ def nvcc() -> str:
         if cand and os.path.exists(cand):
             return cand
     raise RuntimeError("nvcc not found: the CUDA library cannot be built")
+
+
+def check_kernel_registers(src: str, ptxas_log: str) -> None:
+    """Refuse a build whose attention kernel would not launch with the register count its run-time
+    warpgroup split assumes (a smaller count would make the split wait forever)."""
+    current, checked = None, 0
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current and "zyfa_fwd_kernel" in current:
+            if int(m.group(1)) != KERNEL_REGS:
+                raise RuntimeError(f"{src}: {current} uses {m.group(1)} registers, the register split needs "
+                                   f"{KERNEL_REGS}")
+            current = None
+            checked += 1
+    if "kernels" in src and checked == 0:
+        raise RuntimeError(f"{src}: no register report found for the attention kernel")
 
 
 def _inputs_newer(target: str) -> bool:
@@ -45,12 +69,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
-        if verbose:
-            cmd.insert(1, "-Xptxas=-v")
+        cmd = [cc, *ARCH, *FLAGS, "-Xptxas=-v", "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        check_kernel_registers(src, r.stderr)
         if verbose and r.stderr:
             sys.stderr.write(r.stderr)
         return obj

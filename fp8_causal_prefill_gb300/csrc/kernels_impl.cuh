@@ -7,17 +7,17 @@ namespace zyfa {
 
 template <bool FP8, int DQK, int DV>
 int smem_bytes() {
-  return Cfg<FP8, DQK, DV>::kSmemBytes;
+  return Cfg<FP8, DQK, DV, tile_keys<FP8, DQK, DV>()>::kSmemBytes;
 }
 
 template <bool FP8, int DQK, int DV>
 cudaError_t launch_fwd(const LaunchArgs& a) {
-  using C = Cfg<FP8, DQK, DV>;
-  auto kernel = zyfa_fwd_kernel<FP8, DQK, DV>;
+  constexpr int BN = tile_keys<FP8, DQK, DV>();
+  using C = Cfg<FP8, DQK, DV, BN>;
+  auto kernel = zyfa_fwd_kernel<FP8, DQK, DV, BN>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
   Params p;
-  p.q = static_cast<const uint8_t*>(a.q);
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.q_descale = a.q_descale;
   p.k_descale = a.k_descale;
@@ -34,7 +34,7 @@ cudaError_t launch_fwd(const LaunchArgs& a) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = a.stream;
-  return cudaLaunchKernelEx(&cfg, kernel, p, a.tm_q, a.tm_k0, a.tm_k1, a.tm_v);
+  return cudaLaunchKernelEx(&cfg, kernel, p, a.maps);
 }
 
 }  // namespace zyfa

@@ -5,8 +5,12 @@
 
 namespace zyfa {
 
+// 4-D tensor maps over [B][S][heads][D]; *0 move 128-byte chunks of a row, *1 its 64-byte tail chunk.
+struct Maps {
+  CUtensorMap q0, q1, k0, k1, v;
+};
+
 struct LaunchArgs {
-  const void* q;
   void* out;
   const float* q_descale;
   const float* k_descale;
@@ -16,9 +20,15 @@ struct LaunchArgs {
   int num_units;
   int* status;
   int grid;
-  CUtensorMap tm_q, tm_k0, tm_k1, tm_v;
+  Maps maps;
   cudaStream_t stream;
 };
+
+// Keys per K/V tile of an instantiation (the TMA box height of the K and V maps).
+template <bool FP8, int DQK, int DV>
+constexpr int tile_keys() {
+  return (!FP8 && DQK == 192) ? 64 : 128;
+}
 
 // Defined for <true,64,64>, <true,128,128>, <true,192,128> in zyfa_kernels_fp8.cu and for the same
 // head shapes with FP8 = false in zyfa_kernels_bf16.cu.

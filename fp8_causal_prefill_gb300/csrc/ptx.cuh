@@ -62,6 +62,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
 }
 
 // ------------------------------------------------------------------------------------------------
+// warpgroup register reallocation (every warp of the warpgroup executes the same instruction)
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ------------------------------------------------------------------------------------------------
 // proxies / fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -140,6 +152,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
+}
+
+// After tcgen05.wait::ld: tie the loaded registers to the wait so no use is scheduled before it.
+template <int N>
+__device__ __forceinline__ void tmem_ld_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i])::"memory");
 }
 
 __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r) {

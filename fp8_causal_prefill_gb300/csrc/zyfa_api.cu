@@ -75,18 +75,26 @@ zyfa_status_t run(zyfa::LaunchArgs& a, const void* q, const void* k, const void*
   constexpr int es = FP8 ? 1 : 2;
   constexpr int kRowK = DQK * es, kRowV = DV * es;
   constexpr int kChunk = 128 / es;  // elements per 128-byte chunk
+  constexpr int BN = zyfa::tile_keys<FP8, DQK, DV>();
+  constexpr int kRowsQ = 128;
   bool ok = true;
-  // K: 128-byte chunks with the 128-byte swizzle, plus a 64-byte tail chunk with the 64-byte swizzle
-  if (kRowK >= 128) ok &= make_map(&a.tm_k0, k, FP8, DQK, a.H_kv, a.S, a.B, kChunk, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (kRowK % 128 == 64) ok &= make_map(&a.tm_k1, k, FP8, DQK, a.H_kv, a.S, a.B, 64 / es, 64, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (kRowK < 128) a.tm_k0 = a.tm_k1;
-  if (kRowK % 128 != 64) a.tm_k1 = a.tm_k0;
-  // V: MN-major tiles, one swizzle atom per 128 bytes of the value row
-  ok &= make_map(&a.tm_v, v, FP8, DV, a.H_kv, a.S, a.B, kRowV >= 128 ? kChunk : DV, 64,
+  zyfa::Maps& m = a.maps;
+  // Q and K rows: 128-byte chunks with the 128-byte swizzle, a 64-byte tail chunk with the 64-byte one
+  if (kRowK >= 128) {
+    ok &= make_map(&m.q0, q, FP8, DQK, a.H, a.S, a.B, kChunk, kRowsQ, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&m.k0, k, FP8, DQK, a.H_kv, a.S, a.B, kChunk, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (kRowK % 128 == 64) {
+    ok &= make_map(&m.q1, q, FP8, DQK, a.H, a.S, a.B, 64 / es, kRowsQ, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok &= make_map(&m.k1, k, FP8, DQK, a.H_kv, a.S, a.B, 64 / es, BN, CU_TENSOR_MAP_SWIZZLE_64B);
+  }
+  // V: MN-major tiles, one swizzle atom per 128 bytes (or the whole 64-byte row) of the value row
+  ok &= make_map(&m.v, v, FP8, DV, a.H_kv, a.S, a.B, kRowV >= 128 ? kChunk : DV, BN,
                  kRowV >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-  if (!FP8) ok &= make_map(&a.tm_q, q, FP8, DQK, a.H, a.S, a.B, kChunk, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  else a.tm_q = a.tm_v;
   if (!ok) return ZYFA_ERR_CUDA;
+  // maps the instantiation never touches are copies of valid ones
+  if (kRowK < 128) { m.q0 = m.q1; m.k0 = m.k1; }
+  if (kRowK % 128 != 64) { m.q1 = m.q0; m.k1 = m.k0; }
   return zyfa::launch_fwd<FP8, DQK, DV>(a) == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
@@ -135,7 +143,6 @@ zyfa_status_t zyfa_attn_fwd_causal(const void* q, const void* k, const void* v, 
 
   zyfa::LaunchArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.q = q;
   a.out = out;
   const bool fp8 = dtype == ZYFA_DTYPE_E4M3;
   a.q_descale = fp8 ? q_descale : nullptr;

@@ -10,34 +10,37 @@
 //   Lean P: code_ij = clamp(rne(fl32(u_ij + 55.625 - 8e)), 0, 126)  -- one FMA and one conversion;
 //   the block's codes are e4m3 probabilities scaled up by 2^-e; the PV product removes the scale
 //   with an e8m0 block scale factor 2^(e - M) (M: the row's integer reference exponent);
-//   out_i = dv * sum_j w_ij v8_j / sum_j w_ij with the same rounded weights w (the row sum is an
-//   same block-scaled PV MMA, widened by 16 columns whose B operand is a tile of ones: the pages'
+//   out_i = dv * sum_j w_ij v8_j / sum_j w_ij with the same rounded weights w: the row sum comes from
+//   the same block-scaled PV MMA, widened by 16 columns whose B operand is a tile of ones (the pages'
 //   "one extra matrix instruction per block", +16/DV of the PV work).
-// BF16 twin: p_ij = bf16(2^(S_ij*a' - M)), a' = fl32(scale*log2 e), normalised by the sum of the
-// rounded p (same widened PV MMA), no block scaling.
+// BF16 twin: p_ij = bf16(2^(S_ij*a' - M)), a' = fl32(scale*log2 e), normalised by the fp32 sum of the
+// rounded p (accumulated by the softmax threads), no block scaling.
 //
-// Schedule (one persistent CTA per SM, one work unit = (b, h, 256 query rows) = two 128-row tiles):
-//   warp 0      TMA producer: K/V tiles of 64 keys into a ring of shared-memory stages (BF16: Q too)
+// Schedule (one persistent CTA per SM; one work unit = (b, h, 256 query rows) = two 128-row tiles
+// Q0, Q1 that share every K/V tile of BN keys):
+//   warp 0      TMA producer: Q tiles and a ring of K/V stages in shared memory
 //   warp 1      MMA issuer (one thread) and TMEM owner
-//   warps 4..7  softmax warpgroup 0 (query tile 0), warps 8..11 softmax warpgroup 1 (query tile 1)
-// The MMA thread interleaves the tiles, S0(j+1) between PV0(j) and PV1(j), so one warpgroup computes
-// probabilities while the tensor core works on the other tile (the pages' ping-pong, here between
-// two query tiles with mbarrier completion tracking instead of instruction order).
+//   warps 4..7  softmax warpgroup of Q0, warps 8..11 softmax warpgroup of Q1
+// The MMA thread issues, per K/V tile j:  S0(j), PV1(j-1), S1(j), PV0(j).  The two score tiles share
+// one TMEM buffer: a softmax warpgroup copies its scores to registers and releases the buffer at once,
+// so the next score MMA runs while it computes probabilities, and the PV of the other tile keeps the
+// tensor core busy meanwhile (the pages' ping-pong, here between two query tiles with mbarrier
+// completion tracking).  Because S_t(j) is issued after PV_t(j-1), the commit that announces S_t(j)
+// also certifies that PV_t(j-1) is complete: the softmax may then rescale O_t and reuse P_t.
+// Every tcgen05 instruction costs the issuing thread tens of cycles, so score MMAs are 128 keys wide.
 //
-// Tensor memory (512 columns x 128 lanes, lane = query row of the tile):
-//   [  0, 64) S0 (fp32 scores); after the softmax reads it: P0 at 0 (fp8: 16 cols, bf16: 32 cols),
-//             FP8 scale factors of P0 at 32..35, of V (all 1.0) at 48..55
-//   [ 64,128) S1, P1, scale factors of tile 1
-//   [128,128+DV+16) O0 | l0, then O1 | l1   (fp32 accumulators: DV output columns followed by 16
-//             identical columns holding the rounded row sum)
-//   [416,512) Q0, Q1 (FP8 only: e4m3 query rows, DQK/4 columns each)
-// Shared memory per pipeline stage: the K tile, then the V tile (MN-major, 1-2 swizzle atoms) followed
-// by one atom of ones, so the widened PV MMA reads [V | 1] with a single descriptor.
+// Tensor memory (512 columns x 128 lanes; lane = query row of a tile):
+//   [  0,128)            S: fp32 scores of the tile being handed to a softmax warpgroup
+//   [128,128+NO)         O0 (fp32, DV output columns; FP8: then 16 columns of the rounded row sum)
+//   [128+NO,128+2NO)     O1
+//   [416,480)            P tiles (FP8: P0 | P1, e4m3 codes, BN/4 columns each; BF16: one shared tile)
+//   [480,484) [488,492)  e8m0 scale factors of P0, P1 (FP8)   [496,504) scale factors of V (all 1.0)
 #pragma once
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "launch.h"
 #include "ptx.cuh"
 
 namespace zyfa {
@@ -45,67 +48,84 @@ namespace zyfa {
 // Status bits a kernel may set in the library's status word.
 enum : int { kStatusTimeout = 1 };
 
-constexpr int kBlockN = 64;          // keys per K/V tile = keys per scale block
 constexpr int kBlockM = 128;         // query rows per tile
 constexpr int kUnitRows = 2 * kBlockM;
+constexpr int kScaleBlock = 64;      // keys per power-of-two scale block
 constexpr int kThreads = 384;
+// Register split (per thread): the kernel is built for 168 registers x 384 threads; the producer /
+// MMA warpgroup gives registers back so the two softmax warpgroups can hold a 128-key score row.
+// 128 x 56 + 256 x 224 = 384 x 168: the split never asks for more than the launch allotted.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsControl = 56;
+constexpr int kRegsSoftmax = 224;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr int kRescaleBinades = 8;   // lazy reference update threshold (binades)
 constexpr float kLeanPC0 = 55.625f;  // Lean-P constant: code(2^x) = rne(8x + 55.625)
 constexpr long long kWaitLimit = 1ll << 31;  // ~1 s of SM clocks before a wait gives up
+constexpr int kNoExp = -2147483647;  // block exponent of a fully masked block
 
-template <bool FP8, int DQK, int DV>
+template <bool FP8, int DQK, int DV, int BN>
 struct Cfg {
+  static_assert(BN == 64 || BN == 128, "K/V tile of 64 or 128 keys");
   static constexpr int kElem = FP8 ? 1 : 2;
+  // K / Q rows: 128-byte chunks (128-byte swizzle) and at most one 64-byte chunk (64-byte swizzle)
   static constexpr int kRowBytesK = DQK * kElem;
-  static constexpr int kChunks128K = kRowBytesK / 128;                 // 128-byte K-major chunks
-  static constexpr bool kTail64K = (kRowBytesK % 128) == 64;           // one 64-byte chunk
+  static constexpr int kChunks128K = kRowBytesK / 128;
+  static constexpr bool kTail64K = (kRowBytesK % 128) == 64;
   static_assert(kRowBytesK % 64 == 0, "head dim must give whole 64-byte chunks");
-  static constexpr int kKStageBytes = kBlockN * kRowBytesK;
+  static constexpr int kKStageBytes = BN * kRowBytesK;
+  static constexpr int kQTileBytes = kBlockM * kRowBytesK;
+  // V rows (MN-major B operand): atoms of 128-byte (or 64-byte) rows
   static constexpr int kRowBytesV = DV * kElem;
-  static_assert(kRowBytesV == 64 || kRowBytesV % 128 == 0, "value row must be 64 or k*128 bytes");
-  static constexpr int kVAtoms = kRowBytesV >= 128 ? kRowBytesV / 128 : 1;
-  static constexpr int kVAtomBytes = kBlockN * (kRowBytesV >= 128 ? 128 : 64);
-  static constexpr int kVStageBytes = kBlockN * kRowBytesV;                // bytes TMA writes
-  static constexpr int kVRegionBytes = (kVAtoms + 1) * kVAtomBytes;        // + the ones atom
-  static constexpr int kNO = DV + 16;                                      // PV MMA width
-  static constexpr int kQTileBytes = FP8 ? 0 : kBlockM * kRowBytesK;  // BF16 keeps Q in smem
-  static constexpr int kKSteps = kRowBytesK / 32;                      // 32 bytes of K per MMA
+  static constexpr int kVAtomRow = kRowBytesV >= 128 ? 128 : 64;
+  static constexpr int kVAtoms = kRowBytesV / kVAtomRow;
+  static constexpr int kVAtomBytes = BN * kVAtomRow;
+  static constexpr int kVStageBytes = BN * kRowBytesV;
+  static constexpr bool kOnes = FP8;  // FP8: row sum from the widened PV MMA
+  static_assert(!kOnes || kVAtoms == 1, "the shared ones atom needs a single V atom");
+  static constexpr int kOnesBytes = kOnes ? kVAtomBytes : 0;
+  static constexpr int kNO = kOnes ? DV + 16 : DV;  // PV MMA width
+  static constexpr int kKSteps = kRowBytesK / 32;  // 32 bytes of K per MMA
   static constexpr int kKeysPerStep = FP8 ? 32 : 16;
-  static constexpr int kPVSteps = kBlockN / kKeysPerStep;
+  static constexpr int kPVSteps = BN / kKeysPerStep;
+  static constexpr int kPCols = BN * kElem / 4;    // TMEM columns of one P tile
+  static constexpr bool kSharedP = !FP8;
+  // shared memory
   static constexpr int kSmemBudget = 220 * 1024;
-  static constexpr int kFixedBytes = 2 * kQTileBytes + 1024 /*align slack*/;
-  static constexpr int kStageBytes = kKStageBytes + kVRegionBytes;
+  static constexpr int kStageBytes = kKStageBytes + kVStageBytes;
+  static constexpr int kFixedBytes = 2 * kQTileBytes + kOnesBytes + 1024 /*align slack*/;
   static constexpr int kStagesRaw = (kSmemBudget - kFixedBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static_assert(kStages >= 2, "not enough shared memory for two K/V stages");
   static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
-  // TMEM columns of query tile t
-  __device__ static constexpr uint32_t col_s(int t) { return 64u * t; }
+  // tensor memory columns
+  static constexpr uint32_t kColS = 0;
   __device__ static constexpr uint32_t col_o(int t) { return 128u + static_cast<uint32_t>(kNO) * t; }
-  __device__ static constexpr uint32_t col_l(int t) { return col_o(t) + DV; }
-  __device__ static constexpr uint32_t col_q(int t) { return 416u + (DQK / 4) * t; }
-  static_assert(128 + 2 * kNO <= 416, "O accumulators overlap the Q columns");
-  static_assert(!FP8 || 416 + 2 * (DQK / 4) <= 512, "TMEM overflow");
-  static_assert(DV <= 128 && kNO % 16 == 0, "PV MMA width must be a multiple of 16, at most 144");
-  static constexpr uint32_t kColSFA = 32, kColSFB = 48;
+  __device__ static constexpr uint32_t col_p(int t) {
+    return 416u + (kSharedP ? 0u : static_cast<uint32_t>(kPCols) * t);
+  }
+  __device__ static constexpr uint32_t col_sfa(int t) { return 480u + 8u * t; }
+  static constexpr uint32_t kColSFB = 496;
+  static_assert(128 + 2 * kNO <= 416, "O accumulators overlap the P tiles");
+  static_assert(416 + (kSharedP ? 1 : 2) * kPCols <= 480, "P tiles overlap the scale factors");
+  static_assert(kNO % 16 == 0 && kNO <= 256, "PV MMA width");
 };
 
 struct Params {
-  const uint8_t* q;  // [B,S,H,DQK] e4m3 or bf16
   __nv_bfloat16* out;  // [B,S,H,DV]
   const float* q_descale;
   const float* k_descale;
   const float* v_descale;
   int B, S, H, H_kv;
   float softmax_scale;
-  int num_units;     // B*H*ceil(S/256)
-  int* status;       // device status word (timeouts)
+  int num_units;  // B*H*ceil(S/256)
+  int* status;    // device status word (timeouts)
 };
 
 struct __align__(8) SharedCtl {
-  uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
+  uint64_t kv_full[8], kv_empty[8];
   uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2];
-  uint64_t drain;
+  uint64_t s_free, p_free, drain;
   uint32_t tmem_base;
   int abort_;
 };
@@ -133,18 +153,29 @@ __device__ __forceinline__ bool unit_at(const Params& p, int round, Unit& u) {
   return true;
 }
 
-// Number of 64-key tiles tile t of a unit needs (0 if it has no rows).
+// Number of BN-key tiles query tile t of a unit needs (0 if the tile has no rows).
+template <int BN>
 __device__ __forceinline__ int tiles_for(const Params& p, int r0, int t) {
   const int first = r0 + t * kBlockM;
   if (first >= p.S) return 0;
   const int end = min(first + kBlockM, p.S);
-  return (end + kBlockN - 1) / kBlockN;
+  return (end + BN - 1) / BN;
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// max over 64 consecutive values, as a tree of 3-input maxima (short dependency chains)
+__device__ __forceinline__ float max64(const float* s) {
+  float m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    m[i] = fmax3(fmax3(s[8 * i], s[8 * i + 1], s[8 * i + 2]), fmax3(s[8 * i + 3], s[8 * i + 4], s[8 * i + 5]),
+                 fmaxf(s[8 * i + 6], s[8 * i + 7]));
+  return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
 // Two fp32 -> packed f16x2 with negative values clamped to +0; the upper half takes `hi`.
@@ -177,12 +208,25 @@ __device__ __forceinline__ float exp2i(int d) {
   return d < -126 ? 0.0f : __int_as_float((127 + d) << 23);
 }
 
-template <bool FP8, int DQK, int DV>
+// Lean-P codes of the 64 scores of one scale block with exponent e: t = fma(s, a, 55.625 - 8e) scaled
+// by 2^-24, so the f16 subnormal that the rounding conversion produces carries the integer code in
+// its low byte (negative values clamp to 0).  Four codes per 32-bit word, key order = byte order.
+__device__ __forceinline__ void leanp_block(const float* s, float a24, int e, uint32_t (&pw)[16]) {
+  const float c24 = __fmul_rn(kLeanPC0 - 8.0f * static_cast<float>(e), 0x1p-24f);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float t0 = __fmaf_rn(s[4 * i + 0], a24, c24);
+    const float t1 = __fmaf_rn(s[4 * i + 1], a24, c24);
+    const float t2 = __fmaf_rn(s[4 * i + 2], a24, c24);
+    const float t3 = __fmaf_rn(s[4 * i + 3], a24, c24);
+    pw[i] = prmt(cvt_relu_f16x2(t1, t0), cvt_relu_f16x2(t3, t2), 0x6420u);
+  }
+}
+
+template <bool FP8, int DQK, int DV, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    zyfa_fwd_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_k0, const __grid_constant__ CUtensorMap tm_k1,
-                    const __grid_constant__ CUtensorMap tm_v) {
-  using C = Cfg<FP8, DQK, DV>;
+    zyfa_fwd_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  using C = Cfg<FP8, DQK, DV, BN>;
   using namespace ptx;
   extern __shared__ uint8_t smem_raw[];
   __shared__ SharedCtl ctl;
@@ -191,40 +235,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // ---- shared memory carve-up (1024-byte aligned for the 128-byte swizzle) ----
+  // ---- shared memory: [Q0 | Q1 | stage 0 (K|V) | ... | ones atom], 1024-byte aligned ----
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
-  const uint32_t s_q = base;                          // BF16: two Q tiles
-  const uint32_t s_stages = s_q + 2 * C::kQTileBytes; // K/V ring
+  const uint32_t s_q = base;
+  const uint32_t s_stages = s_q + 2 * C::kQTileBytes;
+  // FP8: one atom of e4m3 1.0 above every V stage; the PV descriptor reaches it through its
+  // leading-dimension offset (a positive distance from each stage)
+  const uint32_t s_ones = s_stages + C::kStages * C::kStageBytes;
   auto k_stage = [&](int s) { return s_stages + s * C::kStageBytes; };
-  auto v_stage = [&](int s) { return s_stages + s * C::kStageBytes + C::kKStageBytes; };  // 1024-aligned
+  auto v_stage = [&](int s) { return s_stages + s * C::kStageBytes + C::kKStageBytes; };
 
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(smem_u32(&ctl.k_full[s]), 1);
-      mbar_init(smem_u32(&ctl.k_empty[s]), 1);
-      mbar_init(smem_u32(&ctl.v_full[s]), 1);
-      mbar_init(smem_u32(&ctl.v_empty[s]), 1);
+      mbar_init(smem_u32(&ctl.kv_full[s]), 1);
+      mbar_init(smem_u32(&ctl.kv_empty[s]), 1);
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(smem_u32(&ctl.q_full[t]), FP8 ? 4 : 1);
+      mbar_init(smem_u32(&ctl.q_full[t]), 1);
       mbar_init(smem_u32(&ctl.q_empty[t]), 1);
       mbar_init(smem_u32(&ctl.s_full[t]), 1);
       mbar_init(smem_u32(&ctl.p_full[t]), 4);
       mbar_init(smem_u32(&ctl.o_done[t]), 1);
     }
+    mbar_init(smem_u32(&ctl.s_free), 4);
+    mbar_init(smem_u32(&ctl.p_free), 1);
     mbar_init(smem_u32(&ctl.drain), 1);
     ctl.abort_ = 0;
     fence_mbar_init();
   }
-  {
-    // the ones atom after every V tile: e4m3 1.0 = 0x38, bf16 1.0 = 0x3F80
-    const uint32_t one = FP8 ? 0x38383838u : 0x3F803F80u;
-    for (int st = 0; st < C::kStages; ++st) {
-      uint32_t* o32 = reinterpret_cast<uint32_t*>(base_ptr + (v_stage(st) - base) + C::kVAtoms * C::kVAtomBytes);
-      for (int i = tid; i < C::kVAtomBytes / 4; i += kThreads) o32[i] = one;
-    }
+  if constexpr (C::kOnes) {
+    uint32_t* o32 = reinterpret_cast<uint32_t*>(base_ptr + (s_ones - base));
+    for (int i = tid; i < C::kOnesBytes / 4; i += kThreads) o32[i] = 0x38383838u;  // e4m3 1.0
     fence_proxy_async_smem();
   }
   if (warp == 1) {
@@ -240,57 +283,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 1;
     atomicOr(p.status, kStatusTimeout);
   };
-
   const int hgroup = p.H / p.H_kv;
 
   if (warp == 0) {
     // =========================== TMA producer ===========================
+    regs_dec<kRegsControl>();
     if (lane == 0) {
-      tma_prefetch_desc(&tm_k0);
-      tma_prefetch_desc(&tm_v);
-      if (C::kTail64K) tma_prefetch_desc(&tm_k1);
-      if (!FP8) tma_prefetch_desc(&tm_q);
-      uint32_t k_cnt = 0, v_cnt = 0;  // K / V tiles issued
-      uint32_t q_cnt[2] = {0, 0};      // BF16 Q tiles issued
+      tma_prefetch_desc(&maps.k0);
+      tma_prefetch_desc(&maps.v);
+      tma_prefetch_desc(&maps.q0);
+      uint32_t kv_cnt = 0;
+      uint32_t q_cnt[2] = {0, 0};
       bool ok = true;
       Unit u;
       for (int round = 0; ok && unit_at(p, round, u); ++round) {
         const int hk = u.h / hgroup;
-        const int n0 = tiles_for(p, u.r0, 0), n1 = tiles_for(p, u.r0, 1);
+        const int n0 = tiles_for<BN>(p, u.r0, 0), n1 = tiles_for<BN>(p, u.r0, 1);
         const int nkv = n1 > n0 ? n1 : n0;
-        if (!FP8) {
-          for (int t = 0; t < 2 && ok; ++t) {
-            if ((t == 0 ? n0 : n1) == 0) continue;
-            ok = mbar_wait(smem_u32(&ctl.q_empty[t]), (q_cnt[t] & 1) ^ 1, abort_flag, kWaitLimit);
-            if (!ok) break;
-            const uint32_t bar = smem_u32(&ctl.q_full[t]);
-            mbar_arrive_expect_tx(bar, C::kQTileBytes);
-            for (int c = 0; c < C::kChunks128K; ++c)
-              tma_load_4d(s_q + t * C::kQTileBytes + c * (kBlockM * 128), &tm_q, bar, c * (128 / C::kElem),
-                          u.h, u.r0 + t * kBlockM, u.b);
-            ++q_cnt[t];
-          }
+        for (int t = 0; t < 2 && ok; ++t) {
+          if ((t == 0 ? n0 : n1) == 0) continue;
+          ok = mbar_wait(smem_u32(&ctl.q_empty[t]), (q_cnt[t] & 1) ^ 1, abort_flag, kWaitLimit);
+          if (!ok) break;
+          const uint32_t bar = smem_u32(&ctl.q_full[t]);
+          const uint32_t dst = s_q + t * C::kQTileBytes;
+          mbar_arrive_expect_tx(bar, C::kQTileBytes);
+          for (int c = 0; c < C::kChunks128K; ++c)
+            tma_load_4d(dst + c * (kBlockM * 128), &maps.q0, bar, c * (128 / C::kElem), u.h, u.r0 + t * kBlockM,
+                        u.b);
+          if (C::kTail64K)
+            tma_load_4d(dst + C::kChunks128K * (kBlockM * 128), &maps.q1, bar, C::kChunks128K * (128 / C::kElem),
+                        u.h, u.r0 + t * kBlockM, u.b);
+          ++q_cnt[t];
         }
         for (int j = 0; j < nkv && ok; ++j) {
-          const int st = k_cnt % C::kStages;
-          const uint32_t ph = ((k_cnt / C::kStages) & 1) ^ 1;
-          ok = mbar_wait(smem_u32(&ctl.k_empty[st]), ph, abort_flag, kWaitLimit);
+          const int st = kv_cnt % C::kStages;
+          ok = mbar_wait(smem_u32(&ctl.kv_empty[st]), ((kv_cnt / C::kStages) & 1) ^ 1, abort_flag, kWaitLimit);
           if (!ok) break;
-          const uint32_t kb = smem_u32(&ctl.k_full[st]);
-          mbar_arrive_expect_tx(kb, C::kKStageBytes);
+          const uint32_t bar = smem_u32(&ctl.kv_full[st]);
+          mbar_arrive_expect_tx(bar, C::kKStageBytes + C::kVStageBytes);
           for (int c = 0; c < C::kChunks128K; ++c)
-            tma_load_4d(k_stage(st) + c * (kBlockN * 128), &tm_k0, kb, c * (128 / C::kElem), hk, j * kBlockN, u.b);
+            tma_load_4d(k_stage(st) + c * (BN * 128), &maps.k0, bar, c * (128 / C::kElem), hk, j * BN, u.b);
           if (C::kTail64K)
-            tma_load_4d(k_stage(st) + C::kChunks128K * (kBlockN * 128), &tm_k1, kb,
-                        C::kChunks128K * (128 / C::kElem), hk, j * kBlockN, u.b);
-          ++k_cnt;
-          ok = mbar_wait(smem_u32(&ctl.v_empty[st]), ph, abort_flag, kWaitLimit);
-          if (!ok) break;
-          const uint32_t vb = smem_u32(&ctl.v_full[st]);
-          mbar_arrive_expect_tx(vb, C::kVStageBytes);
+            tma_load_4d(k_stage(st) + C::kChunks128K * (BN * 128), &maps.k1, bar, C::kChunks128K * (128 / C::kElem),
+                        hk, j * BN, u.b);
           for (int c = 0; c < C::kVAtoms; ++c)
-            tma_load_4d(v_stage(st) + c * C::kVAtomBytes, &tm_v, vb, c * (128 / C::kElem), hk, j * kBlockN, u.b);
-          ++v_cnt;
+            tma_load_4d(v_stage(st) + c * C::kVAtomBytes, &maps.v, bar, c * (C::kVAtomRow / C::kElem), hk, j * BN,
+                        u.b);
+          ++kv_cnt;
         }
       }
       if (!ok) {
@@ -298,72 +337,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every load already issued lands before the CTA may exit (its shared memory is released then)
         const int never = 0;
         const uint32_t ns = C::kStages;
-        for (uint32_t i = (k_cnt > ns ? k_cnt - ns : 0); i < k_cnt; ++i)
-          mbar_wait(smem_u32(&ctl.k_full[i % ns]), (i / ns) & 1, &never, kWaitLimit);
-        for (uint32_t i = (v_cnt > ns ? v_cnt - ns : 0); i < v_cnt; ++i)
-          mbar_wait(smem_u32(&ctl.v_full[i % ns]), (i / ns) & 1, &never, kWaitLimit);
+        for (uint32_t i = (kv_cnt > ns ? kv_cnt - ns : 0); i < kv_cnt; ++i)
+          mbar_wait(smem_u32(&ctl.kv_full[i % ns]), (i / ns) & 1, &never, kWaitLimit);
         for (int t = 0; t < 2; ++t)
           if (q_cnt[t] > 0) mbar_wait(smem_u32(&ctl.q_full[t]), (q_cnt[t] - 1) & 1, &never, kWaitLimit);
       }
     }
   } else if (warp == 1) {
     // =========================== MMA issuer ===========================
+    regs_dec<kRegsControl>();
     if (lane == 0) {
-      const uint32_t idesc_s = idesc_dense(FP8 ? kFmtE4M3 : kFmtBF16, FP8 ? kFmtE4M3 : kFmtBF16, false, false,
-                                           kBlockM, kBlockN);
-      uint32_t kv_cnt = 0;
+      const uint32_t fmt = FP8 ? kFmtE4M3 : kFmtBF16;
+      const uint32_t idesc_s = idesc_dense(fmt, fmt, false, false, kBlockM, BN);
+      uint32_t kv_cnt = 0, s_seq = 0;
       uint32_t q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
       bool ok = true;
 
-      auto k_desc = [&](int st, int ks) -> uint64_t {
-        const int off = ks * 32;
-        if (off < C::kChunks128K * 128)
-          return smem_desc(k_stage(st) + (off / 128) * (kBlockN * 128) + (off % 128), 16, 1024, kSwizzle128B);
-        return smem_desc(k_stage(st) + C::kChunks128K * (kBlockN * 128) + (off - C::kChunks128K * 128), 16, 512,
-                         kSwizzle64B);
-      };
+      // S = Q_t K^T for the K tile in stage st (both operands K-major in shared memory)
       auto issue_s = [&](int t, int st) {
-        const uint32_t d = tmem + C::col_s(t);
+        const uint32_t qa = s_q + t * C::kQTileBytes, kb = k_stage(st);
+#pragma unroll
         for (int ks = 0; ks < C::kKSteps; ++ks) {
-          if constexpr (FP8) {
-            mma_f8_ts(d, tmem + C::col_q(t) + ks * 8, k_desc(st, ks), idesc_s, ks > 0);
+          const int off = ks * 32;
+          uint64_t ad, bd;
+          if (off < C::kChunks128K * 128) {
+            ad = smem_desc(qa + (off / 128) * (kBlockM * 128) + (off % 128), 16, 1024, kSwizzle128B);
+            bd = smem_desc(kb + (off / 128) * (BN * 128) + (off % 128), 16, 1024, kSwizzle128B);
           } else {
-            const int off = ks * 32;
-            const uint64_t qd = smem_desc(s_q + t * C::kQTileBytes + (off / 128) * (kBlockM * 128) + (off % 128), 16,
-                                          1024, kSwizzle128B);
-            mma_f16_ss(d, qd, k_desc(st, ks), idesc_s, ks > 0);
+            const int o2 = off - C::kChunks128K * 128;
+            ad = smem_desc(qa + C::kChunks128K * (kBlockM * 128) + o2, 16, 512, kSwizzle64B);
+            bd = smem_desc(kb + C::kChunks128K * (BN * 128) + o2, 16, 512, kSwizzle64B);
           }
+          if constexpr (FP8) mma_f8_ss(tmem + C::kColS, ad, bd, idesc_s, ks > 0);
+          else mma_f16_ss(tmem + C::kColS, ad, bd, idesc_s, ks > 0);
         }
         tc_commit(smem_u32(&ctl.s_full[t]));
       };
-      // O|l += P x [V | 1]: one MMA per K step, DV + 16 columns wide
+      // O_t (| l_t) += P_t x [V | 1]
       auto issue_pv = [&](int t, int st, bool first) {
-        const uint32_t o = tmem + C::col_o(t), pa = tmem + C::col_s(t);
+        const uint32_t o = tmem + C::col_o(t), pa = tmem + C::col_p(t), vb = v_stage(st);
+        const uint32_t lbo = C::kOnes ? (s_ones - vb) : static_cast<uint32_t>(C::kVAtomBytes);
+#pragma unroll
         for (int ks = 0; ks < C::kPVSteps; ++ks) {
-          const uint32_t vaddr = v_stage(st) + ks * C::kKeysPerStep * (C::kRowBytesV >= 128 ? 128 : 64);
-          const uint64_t vd = C::kRowBytesV >= 128 ? smem_desc(vaddr, C::kVAtomBytes, 1024, kSwizzle128B)
-                                                   : smem_desc(vaddr, C::kVAtomBytes, 512, kSwizzle64B);
+          const uint32_t vaddr = vb + ks * C::kKeysPerStep * C::kVAtomRow;
+          const uint64_t vd = C::kVAtomRow == 128 ? smem_desc(vaddr, lbo, 1024, kSwizzle128B)
+                                                  : smem_desc(vaddr, lbo, 512, kSwizzle64B);
           const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
           if constexpr (FP8) {
-            const uint32_t sfa = tmem + C::col_s(t) + C::kColSFA, sfb = tmem + C::col_s(t) + C::kColSFB;
-            mma_mxf8_ts(o, pa + ks * 8, vd, idesc_block_scaled(kFmtE4M3, kFmtE4M3, true, kBlockM, C::kNO, ks, 0), sfa,
-                        sfb, acc);
+            // K step ks covers keys [32ks, 32ks+32): its e8m0 scale is byte ks of the scale word
+            mma_mxf8_ts(o, pa + ks * 8, vd, idesc_block_scaled(kFmtE4M3, kFmtE4M3, true, kBlockM, C::kNO, ks, 0),
+                        tmem + C::col_sfa(t), tmem + C::kColSFB, acc);
           } else {
             mma_f16_ts(o, pa + ks * 8, vd, idesc_dense(kFmtBF16, kFmtBF16, false, true, kBlockM, C::kNO), acc);
           }
         }
-        tc_commit(smem_u32(&ctl.o_done[t]));
+        if (C::kSharedP) tc_commit(smem_u32(&ctl.p_free));
       };
-      auto wait_k = [&](uint32_t cnt) {
-        return mbar_wait(smem_u32(&ctl.k_full[cnt % C::kStages]), (cnt / C::kStages) & 1, abort_flag, kWaitLimit);
+      auto wait_kv = [&](uint32_t cnt) {
+        return mbar_wait(smem_u32(&ctl.kv_full[cnt % C::kStages]), (cnt / C::kStages) & 1, abort_flag, kWaitLimit);
       };
-      auto wait_v = [&](uint32_t cnt) {
-        return mbar_wait(smem_u32(&ctl.v_full[cnt % C::kStages]), (cnt / C::kStages) & 1, abort_flag, kWaitLimit);
+      // the shared S buffer: the s_seq-th score MMA waits until the previous score tile was read
+      auto wait_s_free = [&]() {
+        return s_seq == 0 || mbar_wait(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit);
+      };
+      auto wait_p = [&](int t) {
+        const bool r = mbar_wait(smem_u32(&ctl.p_full[t]), p_cnt[t] & 1, abort_flag, kWaitLimit);
+        ++p_cnt[t];
+        return r;
       };
 
       Unit u;
       for (int round = 0; ok && unit_at(p, round, u); ++round) {
-        const int n[2] = {tiles_for(p, u.r0, 0), tiles_for(p, u.r0, 1)};
+        const int n[2] = {tiles_for<BN>(p, u.r0, 0), tiles_for<BN>(p, u.r0, 1)};
         const int nkv = n[1] > n[0] ? n[1] : n[0];
         for (int t = 0; t < 2 && ok; ++t) {
           if (n[t] == 0) continue;
@@ -371,45 +416,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++q_cnt[t];
         }
         if (!ok) break;
-        tc_fence_after();
-        // prologue: S0(0), S1(0)
-        ok = wait_k(kv_cnt);
-        if (!ok) break;
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (n[t] > 0) {
-            issue_s(t, kv_cnt % C::kStages);
-            if (!FP8 && n[t] == 1) tc_commit(smem_u32(&ctl.q_empty[t]));
+        // order per K/V tile j: S0(j), PV1(j-1), S1(j), PV0(j); one extra pass for PV1(last)
+        for (int j = 0; j <= nkv && ok; ++j) {
+          const uint32_t cur = kv_cnt + j;
+          if (j < nkv && !(ok = wait_kv(cur))) break;
+          if (j < n[0]) {  // S0(j)
+            if (!(ok = wait_s_free())) break;
+            tc_fence_after();
+            issue_s(0, cur % C::kStages);
+            ++s_seq;
+            if (j == n[0] - 1) tc_commit(smem_u32(&ctl.q_empty[0]));
           }
-        tc_commit(smem_u32(&ctl.k_empty[kv_cnt % C::kStages]));
-        for (int j = 0; j < nkv && ok; ++j) {
-          const uint32_t cur = kv_cnt + j, nxt = cur + 1;
-          const bool more = j + 1 < nkv;
-          ok = wait_v(cur);
-          if (!ok) break;
-          bool k_ready = false;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j < n[t]) {
-              ok = mbar_wait(smem_u32(&ctl.p_full[t]), p_cnt[t] & 1, abort_flag, kWaitLimit);
-              if (!ok) break;
-              ++p_cnt[t];
-              tc_fence_after();
-              issue_pv(t, cur % C::kStages, j == 0);
-            }
-            if (t == 1) tc_commit(smem_u32(&ctl.v_empty[cur % C::kStages]));
-            if (more && j + 1 < n[t]) {
-              if (!k_ready) {
-                ok = wait_k(nxt);
-                if (!ok) break;
-                tc_fence_after();
-                k_ready = true;
-              }
-              issue_s(t, nxt % C::kStages);
-              // BF16: last S MMA of this tile issued; its Q tile may be refilled once it completes
-              if (!FP8 && j + 2 == n[t]) tc_commit(smem_u32(&ctl.q_empty[t]));
-            }
+          if (j >= 1 && j - 1 < n[1]) {  // PV1(j-1): the last use of K/V stage j-1
+            if (!(ok = wait_p(1))) break;
+            tc_fence_after();
+            issue_pv(1, (cur - 1) % C::kStages, j == 1);
+            tc_commit(smem_u32(&ctl.kv_empty[(cur - 1) % C::kStages]));
+            if (j == n[1]) tc_commit(smem_u32(&ctl.o_done[1]));
           }
-          if (ok && more) tc_commit(smem_u32(&ctl.k_empty[nxt % C::kStages]));
+          if (j < n[1]) {  // S1(j)
+            if (!(ok = wait_s_free())) break;
+            tc_fence_after();
+            issue_s(1, cur % C::kStages);
+            ++s_seq;
+            if (j == n[1] - 1) tc_commit(smem_u32(&ctl.q_empty[1]));
+          }
+          if (j < n[0]) {  // PV0(j)
+            if (!(ok = wait_p(0))) break;
+            tc_fence_after();
+            issue_pv(0, cur % C::kStages, j == 0);
+            if (j == n[0] - 1) tc_commit(smem_u32(&ctl.o_done[0]));
+            if (n[1] == 0) tc_commit(smem_u32(&ctl.kv_empty[cur % C::kStages]));
+          }
         }
         kv_cnt += nkv;
       }
@@ -419,15 +457,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(smem_u32(&ctl.drain));
       mbar_wait(smem_u32(&ctl.drain), 0, &never, kWaitLimit);
     }
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    regs_dec<kRegsControl>();  // warps 2, 3: idle members of the control warpgroup
+  } else {
     // =========================== softmax warpgroups ===========================
-    const int t = (warp - 4) >> 2;            // query tile of this warpgroup
-    const int quarter = warp & 3;             // TMEM lane quarter of this warp
-    const int rloc = quarter * 32 + lane;     // row within the tile = TMEM lane
+    regs_inc<kRegsSoftmax>();
+    const int t = (warp - 4) >> 2;         // query tile of this warpgroup
+    const int quarter = warp & 3;          // TMEM lane quarter of this warp
+    const int rloc = quarter * 32 + lane;  // row within the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_addr + C::col_s(t);
+    const uint32_t tS = tmem + lane_addr + C::kColS;
     const uint32_t tO = tmem + lane_addr + C::col_o(t);
-    const uint32_t tL = tmem + lane_addr + C::col_l(t);
+    const uint32_t tP = tmem + lane_addr + C::col_p(t);
 
     float a;
     if constexpr (FP8) {
@@ -438,164 +479,175 @@ __global__ void __launch_bounds__(kThreads, 1)
       a = __fmul_rn(p.softmax_scale, 1.4426950408889634f);
     }
     const float out_scale = (FP8 && p.v_descale) ? *p.v_descale : 1.0f;
-    const float a24 = a * 0x1p-24f;  // exact: scales the Lean-P result into f16 subnormal units
+    const float a24 = a * 0x1p-24f;  // exact: scales Lean-P values into f16 subnormal units
+    if constexpr (FP8) {
+      if (t == 0) {
+        // e8m0 scale factors of V (all 1.0), written once; the first PV is issued only after this
+        // warpgroup's first p_full arrival, which releases these stores
+        tmem_st4(tmem + lane_addr + C::kColSFB, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        tmem_st4(tmem + lane_addr + C::kColSFB + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        tmem_wait_st();
+      }
+    }
 
-    uint32_t s_cnt = 0, p_cnt = 0;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    uint32_t pv_base = 0;  // BF16 shared P tile: PV MMAs of all earlier units
     bool ok = true;
     Unit u;
     for (int round = 0; ok && unit_at(p, round, u); ++round) {
-      const int ntiles = tiles_for(p, u.r0, t);
-      if (ntiles == 0) continue;
-      const int row0 = u.r0 + t * kBlockM;   // first row of the tile
+      const int n0 = tiles_for<BN>(p, u.r0, 0), n1 = tiles_for<BN>(p, u.r0, 1);
+      const int ntiles = t == 0 ? n0 : n1;
+      if (ntiles == 0) {
+        pv_base += n0 + n1;
+        continue;
+      }
+      const int row0 = u.r0 + t * kBlockM;  // first row of the tile
       const int row = row0 + rloc;
       const bool row_ok = row < p.S;
-      if constexpr (FP8) {
-        // Q row -> TMEM (zeros past the end of the sequence)
-        uint32_t w[32];
-        const uint4* qrow = reinterpret_cast<const uint4*>(
-            p.q + ((static_cast<size_t>(u.b) * p.S + (row_ok ? row : 0)) * p.H + u.h) * DQK);
-        constexpr int kVec = DQK / 16;
-        constexpr int kFirst = kVec < 8 ? kVec : 8;
-#pragma unroll
-        for (int i = 0; i < kFirst; ++i) {
-          uint4 x = row_ok ? __ldg(qrow + i) : make_uint4(0, 0, 0, 0);
-          w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
-        }
-        if constexpr (DQK == 64) {
-          uint32_t w16[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w16[i] = w[i];
-          tmem_st16(tmem + lane_addr + C::col_q(t), w16);
-        } else {
-          tmem_st32(tmem + lane_addr + C::col_q(t), w);
-          if constexpr (DQK == 192) {
-            uint32_t w16[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 x = row_ok ? __ldg(qrow + 8 + i) : make_uint4(0, 0, 0, 0);
-              w16[4 * i] = x.x; w16[4 * i + 1] = x.y; w16[4 * i + 2] = x.z; w16[4 * i + 3] = x.w;
-            }
-            tmem_st16(tmem + lane_addr + C::col_q(t) + 32, w16);
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl.q_full[t]));
-      }
 
       int m_ref = 0;
+      float l_bf16 = 0.0f;  // BF16: fp32 sum of the rounded probabilities of this row
       for (int j = 0; j < ntiles; ++j) {
         ok = mbar_wait(smem_u32(&ctl.s_full[t]), s_cnt & 1, abort_flag, kWaitLimit);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         ++s_cnt;
         tc_fence_after();
-        float s[64];
+        float s[BN];
         {
-          uint32_t r[32];
-          tmem_ld32(tS, r);
-          tmem_wait_ld();
+          uint32_t r[BN];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
-          tmem_ld32(tS + 32, r);
+          for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
           tmem_wait_ld();
+          tmem_ld_fence(r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(r[i]);
+          for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r[i]);
         }
-        const int key0 = j * kBlockN;
-        if (key0 + kBlockN - 1 > row0) {  // tile touches the diagonal: mask keys after the row
+        // the scores are in registers: release the S buffer for the next score MMA
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl.s_free));
+
+        const int key0 = j * BN;
+        if (key0 + BN - 1 > row0) {  // tile touches the diagonal: mask keys after the row
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
+          for (int i = 0; i < BN; ++i)
             if (key0 + i > row) s[i] = -INFINITY;
         }
-        float mx = fmax3(s[0], s[1], s[2]);
+        constexpr int kNB = BN / kScaleBlock;
+        int e[kNB];
+        int e_top = kNoExp;
 #pragma unroll
-        for (int i = 3; i < 63; i += 2) mx = fmax3(mx, s[i], s[i + 1]);
-        mx = fmaxf(mx, s[63]);
-
-        // block exponent (FP8: ceil(max u / 8); BF16: ceil(max log2-score)) and lazy reference update
-        const bool empty = mx == -INFINITY;
-        int e;
-        if constexpr (FP8) e = empty ? 0 : static_cast<int>(ceilf(__fmul_rn(mx, a) * 0.125f));
-        else e = empty ? 0 : static_cast<int>(ceilf(__fmul_rn(mx, a)));
+        for (int b = 0; b < kNB; ++b) {
+          // block exponent (FP8: ceil(max u / 8); BF16: ceil(max log2-score))
+          const float mx = max64(s + 64 * b);
+          const bool empty = mx == -INFINITY;
+          if constexpr (FP8) e[b] = empty ? kNoExp : static_cast<int>(ceilf(__fmul_rn(mx, a) * 0.125f));
+          else e[b] = empty ? kNoExp : static_cast<int>(ceilf(__fmul_rn(mx, a)));
+          e_top = max(e_top, e[b]);
+        }
         if (j == 0) {
-          m_ref = e;
+          m_ref = e_top;  // key 0 is visible from every row, so e_top is finite
         } else {
-          const bool need = !empty && e > m_ref + kRescaleBinades;
+          const bool need = e_top > m_ref + kRescaleBinades;
           if (__any_sync(0xffffffffu, need)) {
-            // the previous PV into this tile's accumulators must be complete before rescaling
-            ok = mbar_wait(smem_u32(&ctl.o_done[t]), (p_cnt - 1) & 1, abort_flag, kWaitLimit);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
-            const float f = need ? exp2i(m_ref - e) : 1.0f;
-            uint32_t r[32];
+            // O_t is stable: the score MMA just received was issued after the previous PV of tile t
+            const float f = need ? exp2i(m_ref - e_top) : 1.0f;
 #pragma unroll
             for (int c = 0; c < DV / 32; ++c) {
+              uint32_t r[32];
               tmem_ld32(tO + 32 * c, r);
               tmem_wait_ld();
+              tmem_ld_fence(r);
 #pragma unroll
               for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
               tmem_st32(tO + 32 * c, r);
             }
-            uint32_t lv;
-            tmem_ld1(tL, lv);
-            tmem_wait_ld();
-            tmem_st1(tL, __float_as_uint(__uint_as_float(lv) * f));
-            tmem_wait_st();
-            if (need) m_ref = e;
+            if constexpr (FP8) {
+              uint32_t lv[1];
+              tmem_ld1(tO + DV, lv[0]);
+              tmem_wait_ld();
+              tmem_ld_fence(lv);
+              tmem_st1(tO + DV, __float_as_uint(__uint_as_float(lv[0]) * f));
+            } else {
+              l_bf16 *= f;
+            }
+            if (need) m_ref = e_top;
           }
         }
 
         if constexpr (FP8) {
-          // Lean P: t = fma(s, a, 55.625 - 8e) in units of 2^-24, so the f16 subnormal produced by
-          // the rounding conversion carries the integer code in its low byte (negative -> 0).
-          const float c24 = __fmul_rn(kLeanPC0 - 8.0f * static_cast<float>(e), 0x1p-24f);
-          uint32_t pw[16];
+          uint32_t sfw = 0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float t0 = __fmaf_rn(s[4 * i + 0], a24, c24);
-            const float t1 = __fmaf_rn(s[4 * i + 1], a24, c24);
-            const float t2 = __fmaf_rn(s[4 * i + 2], a24, c24);
-            const float t3 = __fmaf_rn(s[4 * i + 3], a24, c24);
-            pw[i] = prmt(cvt_relu_f16x2(t1, t0), cvt_relu_f16x2(t3, t2), 0x6420u);
+          for (int b = 0; b < kNB; ++b) {
+            const int eb = e[b] == kNoExp ? m_ref : e[b];
+            uint32_t pw[16];
+            leanp_block(s + 64 * b, a24, eb, pw);
+            tmem_st16(tP + 16 * b, pw);
+            int sf = 127 + eb - m_ref;
+            sf = sf < 0 ? 0 : (sf > 254 ? 254 : sf);
+            // two 32-key MMA steps per 64-key block: bytes 2b and 2b+1 of the scale word
+            sfw |= static_cast<uint32_t>(sf) * (0x0101u << (16 * b));
           }
-          int sf = 127 + e - m_ref;
-          sf = sf < 0 ? 0 : (sf > 254 ? 254 : sf);
-          const uint32_t sfw = static_cast<uint32_t>(sf) * 0x01010101u;
-          tmem_st16(tS, pw);
-          tmem_st4(tS + C::kColSFA, sfw, sfw, sfw, sfw);
-          tmem_st4(tS + C::kColSFB, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-          tmem_st4(tS + C::kColSFB + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          if (kNB == 1) sfw |= sfw << 16;
+          tmem_st4(tmem + lane_addr + C::col_sfa(t), sfw, sfw, sfw, sfw);
         } else {
+          if constexpr (C::kSharedP) {
+            // the shared P tile is free once the PV just before this one (in issue order) completed:
+            // per unit the PV order is PV0(0), PV1(0), PV0(1), PV1(1), ..., then PV1 of the tail tiles
+            // (a unit whose second tile is empty issues PV0(0), PV0(1), ...)
+            const uint32_t k = pv_base + (n1 == 0 ? j : (j < n0 ? 2 * j + t : n0 + j));
+            if (k > 0) {
+              ok = mbar_wait(smem_u32(&ctl.p_free), (k - 1) & 1, abort_flag, kWaitLimit);
+              if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            }
+            tc_fence_after();
+          }
           const float negm = -static_cast<float>(m_ref);
-          uint32_t pw[32];
+          float lacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            pw[i] = cvt_bf16x2(ex2(__fmaf_rn(s[2 * i + 1], a, negm)), ex2(__fmaf_rn(s[2 * i], a, negm)));
-          tmem_st32(tS, pw);
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t pw[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int k2 = 32 * c + 2 * i;
+              pw[i] = cvt_bf16x2(ex2(__fmaf_rn(s[k2 + 1], a, negm)), ex2(__fmaf_rn(s[k2], a, negm)));
+              lacc[i & 3] += __uint_as_float(pw[i] << 16) + __uint_as_float(pw[i] & 0xFFFF0000u);
+            }
+            tmem_st16(tP + 16 * c, pw);
+          }
+          l_bf16 += (lacc[0] + lacc[1]) + (lacc[2] + lacc[3]);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl.p_full[t]));
-        ++p_cnt;
       }
       if (!ok) break;
+      pv_base += n0 + n1;
 
       // epilogue: out = O * (dv / l) -> bf16
-      ok = mbar_wait(smem_u32(&ctl.o_done[t]), (p_cnt - 1) & 1, abort_flag, kWaitLimit);
+      ok = mbar_wait(smem_u32(&ctl.o_done[t]), o_cnt & 1, abort_flag, kWaitLimit);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ++o_cnt;
       tc_fence_after();
-      uint32_t lv;
-      tmem_ld1(tL, lv);
-      tmem_wait_ld();
-      const float inv = __fdiv_rn(out_scale, __uint_as_float(lv));
+      float l;
+      if constexpr (FP8) {
+        uint32_t lv[1];
+        tmem_ld1(tO + DV, lv[0]);
+        tmem_wait_ld();
+        tmem_ld_fence(lv);
+        l = __uint_as_float(lv[0]);
+      } else {
+        l = l_bf16;
+      }
+      const float inv = __fdiv_rn(out_scale, l);
       __nv_bfloat16* orow = p.out + ((static_cast<size_t>(u.b) * p.S + (row_ok ? row : 0)) * p.H + u.h) * DV;
 #pragma unroll
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tO + 32 * c, r);
         tmem_wait_ld();
+        tmem_ld_fence(r);
         uint32_t packed[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)

@@ -31,6 +31,8 @@ SMALL = [
     Shape(1, 255, 2, 2, 128, 128),
     Shape(1, 256, 2, 2, 128, 128),
     Shape(1, 257, 4, 2, 128, 128),
+    Shape(1, 385, 2, 1, 128, 128),
+    Shape(2, 520, 2, 2, 128, 128),
     Shape(2, 383, 4, 1, 128, 128),
     Shape(1, 1000, 4, 4, 128, 128),
     Shape(1, 256, 2, 2, 64, 64),
@@ -38,6 +40,7 @@ SMALL = [
     Shape(1, 1, 2, 2, 192, 128),
     Shape(1, 130, 2, 2, 192, 128),
     Shape(1, 513, 2, 1, 192, 128),
+    Shape(1, 300, 4, 4, 192, 128),
     Shape(1, 2048, 4, 1, 128, 128, "mistral"),
 ]
 
@@ -51,13 +54,13 @@ def _id(s):
 def test_small_shapes_full_compare(shape, dtype):
     p = make_problem(shape, seed=shape.S + 17 * shape.H)
     out = run_gpu(p, dtype)
+    assert zyfa_check_errors() == 0
     got = select(out)
     ref = oracle_out(p, dtype)
     assert np.all(np.isfinite(got))
     err = O.rel_l2(got, ref)
     assert err <= TOL[dtype], err
     assert per_row_rel(got, ref).max() <= ROW_TOL[dtype]
-    assert zyfa_check_errors() == 0
 
 
 @pytest.mark.parametrize("dtype", ["fp8", "bf16"])
