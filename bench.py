@@ -56,6 +56,16 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_source_hash():
+    """Hash of the kernel sources; recorded ncu traffic counts only while it matches."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("zyfa_fwd.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "fp8_causal_prefill_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def shape_for(args):
     from fp8_causal_prefill_gb300.inputs import CONFIGS, Shape
     sh = CONFIGS[args.config]
@@ -305,7 +315,7 @@ def main():
             with open(tpath) as f:
                 td = json.load(f)
             key = f"{args.dtype}:{args.config}"
-            if key in td and not args.heads:
+            if key in td and not args.heads and td[key].get("kernel_sha256") == kernel_source_hash():
                 traffic = td[key].get("bytes_per_launch")
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -327,7 +337,7 @@ def main():
         }
         if e2e is not None:
             line["e2e"] = e2e
-        if not args.no_cpu and world >= 1:
+        if not args.no_cpu and world == 1:
             line["cpu_baseline"] = cpu_oracle_sample(p, args.dtype, args.cpu_seconds)
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -21,7 +21,8 @@ ZYFA_DTYPE_E4M3 = 0
 ZYFA_DTYPE_BF16 = 1
 STATUS = {0: "ZYFA_OK", 1: "ZYFA_ERR_INVALID_ARG", 2: "ZYFA_ERR_UNSUPPORTED", 3: "ZYFA_ERR_MISALIGNED",
           4: "ZYFA_ERR_CUDA", 5: "ZYFA_ERR_TIMEOUT"}
-EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_check_errors", "zyfa_status_string", "zyfa_kernel_launches")
+EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_check_errors", "zyfa_status_string", "zyfa_kernel_launches",
+            "zyfa_selftest_stalled_pipeline")
 
 
 class ZyfaError(RuntimeError):
@@ -46,6 +47,8 @@ def load_library() -> ctypes.CDLL:
         vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.zyfa_attn_fwd_causal.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, vp, vp, vp]
         lib.zyfa_attn_fwd_causal.restype = ci
+        lib.zyfa_selftest_stalled_pipeline.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp]
+        lib.zyfa_selftest_stalled_pipeline.restype = ci
         lib.zyfa_check_errors.argtypes = [vp]
         lib.zyfa_check_errors.restype = ci
         lib.zyfa_status_string.argtypes = [ci]
@@ -63,6 +66,13 @@ def zyfa_attn_fwd_causal(q: int, k: int, v: int, out: int, B: int, S: int, H: in
     lib = load_library()
     return lib.zyfa_attn_fwd_causal(q, k, v, out, B, S, H, H_kv, D_qk, D_v, float(softmax_scale), dtype,
                                     q_descale or None, k_descale or None, v_descale or None, stream or None)
+
+
+def zyfa_selftest_stalled_pipeline(q: int, k: int, v: int, out: int, B: int, S: int, H: int, H_kv: int, D_qk: int,
+                                   D_v: int, dtype: int, stream: int = 0) -> int:
+    """Enqueue the kernel with its loads withheld (tests of the timeout path); returns the status code."""
+    return load_library().zyfa_selftest_stalled_pipeline(q, k, v, out, B, S, H, H_kv, D_qk, D_v, dtype,
+                                                         stream or None)
 
 
 def zyfa_check_errors(stream: int = 0) -> int:

@@ -29,6 +29,7 @@ cudaError_t launch_fwd(const LaunchArgs& a) {
   p.softmax_scale = a.softmax_scale;
   p.num_units = a.num_units;
   p.status = a.status;
+  p.stall_loads = a.stall_loads;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(kThreads);

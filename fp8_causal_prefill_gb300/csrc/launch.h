@@ -19,6 +19,7 @@ struct LaunchArgs {
   float softmax_scale;
   int num_units;
   int* status;
+  int stall_loads;  // nonzero only for the stalled-pipeline self-test
   int grid;
   Maps maps;
   cudaStream_t stream;

@@ -116,10 +116,15 @@ const char* zyfa_status_string(zyfa_status_t s) {
 
 int zyfa_kernel_launches(int B, int S, int H) { return (B > 0 && S > 0 && H > 0) ? 1 : 0; }
 
-zyfa_status_t zyfa_attn_fwd_causal(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
-                                   int H_kv, int D_qk, int D_v, float softmax_scale, zyfa_dtype_t dtype,
-                                   const float* q_descale, const float* k_descale, const float* v_descale,
-                                   cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of the entry points: validation, tensor maps, launch.  stall_loads != 0 makes the
+// kernel's producer withhold every load (the self-test of the timeout path).
+zyfa_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int S, int H, int H_kv,
+                       int D_qk, int D_v, float softmax_scale, zyfa_dtype_t dtype, const float* q_descale,
+                       const float* k_descale, const float* v_descale, cudaStream_t stream, int stall_loads) {
   if (B < 1 || H < 1 || H_kv < 1 || S < 0 || H % H_kv != 0) return ZYFA_ERR_INVALID_ARG;
   if (dtype != ZYFA_DTYPE_E4M3 && dtype != ZYFA_DTYPE_BF16) return ZYFA_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale) || softmax_scale < 0.0f) return ZYFA_ERR_INVALID_ARG;
@@ -157,6 +162,7 @@ zyfa_status_t zyfa_attn_fwd_causal(const void* q, const void* k, const void* v, 
   a.status = status;
   a.grid = static_cast<int>(units < nsm ? units : nsm);
   a.stream = stream;
+  a.stall_loads = stall_loads;
   if (fp8) {
     if (D_qk == 64) return run<true, 64, 64>(a, q, k, v);
     if (D_qk == 128) return run<true, 128, 128>(a, q, k, v);
@@ -165,6 +171,24 @@ zyfa_status_t zyfa_attn_fwd_causal(const void* q, const void* k, const void* v, 
   if (D_qk == 64) return run<false, 64, 64>(a, q, k, v);
   if (D_qk == 128) return run<false, 128, 128>(a, q, k, v);
   return run<false, 192, 128>(a, q, k, v);
+}
+
+}  // namespace
+
+extern "C" {
+
+zyfa_status_t zyfa_attn_fwd_causal(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
+                                   int H_kv, int D_qk, int D_v, float softmax_scale, zyfa_dtype_t dtype,
+                                   const float* q_descale, const float* k_descale, const float* v_descale,
+                                   cudaStream_t stream) {
+  return attn_fwd(q, k, v, out, B, S, H, H_kv, D_qk, D_v, softmax_scale, dtype, q_descale, k_descale, v_descale,
+                  stream, 0);
+}
+
+zyfa_status_t zyfa_selftest_stalled_pipeline(const void* q, const void* k, const void* v, void* out, int B, int S,
+                                             int H, int H_kv, int D_qk, int D_v, zyfa_dtype_t dtype,
+                                             cudaStream_t stream) {
+  return attn_fwd(q, k, v, out, B, S, H, H_kv, D_qk, D_v, 0.0f, dtype, nullptr, nullptr, nullptr, stream, 1);
 }
 
 zyfa_status_t zyfa_check_errors(cudaStream_t stream) {

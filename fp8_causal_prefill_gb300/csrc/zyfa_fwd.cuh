@@ -120,6 +120,7 @@ struct Params {
   float softmax_scale;
   int num_units;  // B*H*ceil(S/256)
   int* status;    // device status word (timeouts)
+  int stall_loads;  // self-test of the timeout path: the producer withholds every load
 };
 
 struct __align__(8) SharedCtl {
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // =========================== TMA producer ===========================
     regs_dec<kRegsControl>();
-    if (lane == 0) {
+    if (lane == 0 && !p.stall_loads) {
       tma_prefetch_desc(&maps.k0);
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.q0);

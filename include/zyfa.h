@@ -81,6 +81,22 @@ zyfa_status_t zyfa_attn_fwd_causal(const void* q, const void* k, const void* v, 
  */
 zyfa_status_t zyfa_check_errors(cudaStream_t stream);
 
+/*
+ * zyfa_selftest_stalled_pipeline - exercise the timeout path without faulting or hanging the GPU.
+ *
+ * Enqueues the same kernel as zyfa_attn_fwd_causal (same arguments, default softmax scale, no
+ * descales) with its load-issuing warp told to withhold every load.  Every other role then waits on
+ * a barrier that never completes; each wait is bounded (about 2^31 SM clocks, roughly one second),
+ * after which the kernel records ZYFA_ERR_TIMEOUT in the status word, waits for nothing it has in
+ * flight, releases its tensor memory and returns, leaving the CUDA context usable.  `out` is not
+ * written.  Returns the same argument errors as zyfa_attn_fwd_causal, else ZYFA_OK once enqueued;
+ * the following zyfa_check_errors() then returns ZYFA_ERR_TIMEOUT.  For tests of error handling
+ * only.  The pages describe no such call; it belongs to this library's failure detection.
+ */
+zyfa_status_t zyfa_selftest_stalled_pipeline(const void* q, const void* k, const void* v, void* out, int B, int S,
+                                             int H, int H_kv, int D_qk, int D_v, zyfa_dtype_t dtype,
+                                             cudaStream_t stream);
+
 /* zyfa_status_string - static, human-readable name of a status code (never NULL). */
 const char* zyfa_status_string(zyfa_status_t status);
 
