@@ -61,6 +61,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
   }
 }
 
+// One lane of a converged warp (the lowest active one) gets true.  Roles that issue single-thread
+// instructions (TMA copies, tcgen05.mma, tcgen05.commit) run as whole warps and issue under this
+// predicate, so the operands they compute stay warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+  return pred != 0;
+}
+
 // ------------------------------------------------------------------------------------------------
 // warpgroup register reallocation (every warp of the warpgroup executes the same instruction)
 

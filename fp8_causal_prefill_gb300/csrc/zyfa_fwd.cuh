@@ -19,14 +19,17 @@
 // Schedule (one persistent CTA per SM; one work unit = (b, h, 256 query rows) = two 128-row tiles
 // Q0, Q1 that share every K/V tile of BN keys):
 //   warp 0      TMA producer: Q tiles and a ring of K/V stages in shared memory
-//   warp 1      MMA issuer (one thread) and TMEM owner
+//   warp 1      MMA issuer (the whole warp runs the loop, one elected lane issues) and TMEM owner
 //   warps 4..7  softmax warpgroup of Q0, warps 8..11 softmax warpgroup of Q1
-// The MMA thread issues, per K/V tile j:  S0(j), PV1(j-1), S1(j), PV0(j).  The two score tiles share
-// one TMEM buffer: a softmax warpgroup copies its scores to registers and releases the buffer at once,
-// so the next score MMA runs while it computes probabilities, and the PV of the other tile keeps the
-// tensor core busy meanwhile (the pages' ping-pong, here between two query tiles with mbarrier
-// completion tracking).  Because S_t(j) is issued after PV_t(j-1), the commit that announces S_t(j)
-// also certifies that PV_t(j-1) is complete: the softmax may then rescale O_t and reuse P_t.
+// The two score tiles share one TMEM buffer, filled in the order S0(0), S1(0), S0(1), S1(1), ...: a
+// softmax warpgroup copies its scores to registers and releases the buffer at once, and the next
+// score MMA is issued as soon as that release is seen.  The release also tells the MMA thread that
+// the warpgroup's previous P is in TMEM, so PV_t(j-1) is issued right after the score MMA that follows
+// the read of S_t(j): score MMAs never wait for a softmax computation, and the PV of one tile keeps
+// the tensor core busy while the other tile's scores are handed over (the pages' ping-pong, here
+// between two query tiles with mbarrier completion tracking).  A warpgroup may rescale O_t or
+// overwrite P_t once the previous PV of its tile completed: the completion of its next score tile,
+// issued after that PV, certifies it; the last two PVs of a query tile also commit to pv_done.
 // Every tcgen05 instruction costs the issuing thread tens of cycles, so score MMAs are 128 keys wide.
 //
 // Tensor memory (512 columns x 128 lanes; lane = query row of a tile):
@@ -54,10 +57,10 @@ constexpr int kScaleBlock = 64;      // keys per power-of-two scale block
 constexpr int kThreads = 384;
 // Register split (per thread): the kernel is built for 168 registers x 384 threads; the producer /
 // MMA warpgroup gives registers back so the two softmax warpgroups can hold a 128-key score row.
-// 128 x 56 + 256 x 224 = 384 x 168: the split never asks for more than the launch allotted.
+// 128 x 72 + 256 x 208 <= 384 x 168: the split never asks for more than the launch allotted.
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsControl = 56;
-constexpr int kRegsSoftmax = 224;
+constexpr int kRegsControl = 72;
+constexpr int kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr int kRescaleBinades = 8;   // lazy reference update threshold (binades)
 constexpr float kLeanPC0 = 55.625f;  // Lean-P constant: code(2^x) = rne(8x + 55.625)
@@ -89,7 +92,6 @@ struct Cfg {
   static constexpr int kKeysPerStep = FP8 ? 32 : 16;
   static constexpr int kPVSteps = BN / kKeysPerStep;
   static constexpr int kPCols = BN * kElem / 4;    // TMEM columns of one P tile
-  static constexpr bool kSharedP = !FP8;
   // shared memory
   static constexpr int kSmemBudget = 220 * 1024;
   static constexpr int kStageBytes = kKStageBytes + kVStageBytes;
@@ -101,13 +103,20 @@ struct Cfg {
   // tensor memory columns
   static constexpr uint32_t kColS = 0;
   __device__ static constexpr uint32_t col_o(int t) { return 128u + static_cast<uint32_t>(kNO) * t; }
-  __device__ static constexpr uint32_t col_p(int t) {
-    return 416u + (kSharedP ? 0u : static_cast<uint32_t>(kPCols) * t);
-  }
+  // P tiles: FP8 [416,448) [448,480) below the scale factors; BF16 [384,448) [448,512)
+  static constexpr uint32_t kColP = FP8 ? 416u : 384u;
+  __device__ static constexpr uint32_t col_p(int t) { return kColP + static_cast<uint32_t>(kPCols) * t; }
   __device__ static constexpr uint32_t col_sfa(int t) { return 480u + 8u * t; }
   static constexpr uint32_t kColSFB = 496;
-  static_assert(128 + 2 * kNO <= 416, "O accumulators overlap the P tiles");
-  static_assert(416 + (kSharedP ? 1 : 2) * kPCols <= 480, "P tiles overlap the scale factors");
+  static_assert(128 + 2 * kNO <= static_cast<int>(kColP), "O accumulators overlap the P tiles");
+  static_assert(kColP + 2 * kPCols <= (FP8 ? 480u : 512u), "P tiles overlap the scale factors");
+  // Issue order after a score tile is seen read: with three or more K/V stages the next score MMA
+  // goes first (it gates a softmax warpgroup); with two, the PV goes first, because the next score
+  // MMA may need the stage that PV releases.
+  static constexpr bool kScoreFirst = kStages >= 3;
+  // The last PV of query tile 0 waits for the end of the unit, while tile 1 may still need up to
+  // kBlockM / BN more K/V tiles: the ring must hold them without that PV's stage.
+  static_assert(kStages > kBlockM / BN, "K/V ring too short for the PV lag");
   static_assert(kNO % 16 == 0 && kNO <= 256, "PV MMA width");
 };
 
@@ -125,8 +134,8 @@ struct Params {
 
 struct __align__(8) SharedCtl {
   uint64_t kv_full[8], kv_empty[8];
-  uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2];
-  uint64_t s_free, p_free, drain;
+  uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], pv_done[2];
+  uint64_t s_free, drain;
   uint32_t tmem_base;
   int abort_;
 };
@@ -258,10 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl.q_empty[t]), 1);
       mbar_init(smem_u32(&ctl.s_full[t]), 1);
       mbar_init(smem_u32(&ctl.p_full[t]), 4);
-      mbar_init(smem_u32(&ctl.o_done[t]), 1);
+      mbar_init(smem_u32(&ctl.pv_done[t]), 1);
     }
     mbar_init(smem_u32(&ctl.s_free), 4);
-    mbar_init(smem_u32(&ctl.p_free), 1);
     mbar_init(smem_u32(&ctl.drain), 1);
     ctl.abort_ = 0;
     fence_mbar_init();
@@ -289,10 +297,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // =========================== TMA producer ===========================
     regs_dec<kRegsControl>();
-    if (lane == 0 && !p.stall_loads) {
-      tma_prefetch_desc(&maps.k0);
-      tma_prefetch_desc(&maps.v);
-      tma_prefetch_desc(&maps.q0);
+    if (!p.stall_loads) {
+      const bool leader = elect_one();
+      if (leader) {
+        tma_prefetch_desc(&maps.k0);
+        tma_prefetch_desc(&maps.v);
+        tma_prefetch_desc(&maps.q0);
+      }
       uint32_t kv_cnt = 0;
       uint32_t q_cnt[2] = {0, 0};
       bool ok = true;
@@ -307,13 +318,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           const uint32_t bar = smem_u32(&ctl.q_full[t]);
           const uint32_t dst = s_q + t * C::kQTileBytes;
-          mbar_arrive_expect_tx(bar, C::kQTileBytes);
-          for (int c = 0; c < C::kChunks128K; ++c)
-            tma_load_4d(dst + c * (kBlockM * 128), &maps.q0, bar, c * (128 / C::kElem), u.h, u.r0 + t * kBlockM,
-                        u.b);
-          if (C::kTail64K)
-            tma_load_4d(dst + C::kChunks128K * (kBlockM * 128), &maps.q1, bar, C::kChunks128K * (128 / C::kElem),
-                        u.h, u.r0 + t * kBlockM, u.b);
+          if (leader) {
+            mbar_arrive_expect_tx(bar, C::kQTileBytes);
+            for (int c = 0; c < C::kChunks128K; ++c)
+              tma_load_4d(dst + c * (kBlockM * 128), &maps.q0, bar, c * (128 / C::kElem), u.h, u.r0 + t * kBlockM,
+                          u.b);
+            if (C::kTail64K)
+              tma_load_4d(dst + C::kChunks128K * (kBlockM * 128), &maps.q1, bar, C::kChunks128K * (128 / C::kElem),
+                          u.h, u.r0 + t * kBlockM, u.b);
+          }
           ++q_cnt[t];
         }
         for (int j = 0; j < nkv && ok; ++j) {
@@ -321,20 +334,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(smem_u32(&ctl.kv_empty[st]), ((kv_cnt / C::kStages) & 1) ^ 1, abort_flag, kWaitLimit);
           if (!ok) break;
           const uint32_t bar = smem_u32(&ctl.kv_full[st]);
-          mbar_arrive_expect_tx(bar, C::kKStageBytes + C::kVStageBytes);
-          for (int c = 0; c < C::kChunks128K; ++c)
-            tma_load_4d(k_stage(st) + c * (BN * 128), &maps.k0, bar, c * (128 / C::kElem), hk, j * BN, u.b);
-          if (C::kTail64K)
-            tma_load_4d(k_stage(st) + C::kChunks128K * (BN * 128), &maps.k1, bar, C::kChunks128K * (128 / C::kElem),
-                        hk, j * BN, u.b);
-          for (int c = 0; c < C::kVAtoms; ++c)
-            tma_load_4d(v_stage(st) + c * C::kVAtomBytes, &maps.v, bar, c * (C::kVAtomRow / C::kElem), hk, j * BN,
-                        u.b);
+          if (leader) {
+            mbar_arrive_expect_tx(bar, C::kKStageBytes + C::kVStageBytes);
+            for (int c = 0; c < C::kChunks128K; ++c)
+              tma_load_4d(k_stage(st) + c * (BN * 128), &maps.k0, bar, c * (128 / C::kElem), hk, j * BN, u.b);
+            if (C::kTail64K)
+              tma_load_4d(k_stage(st) + C::kChunks128K * (BN * 128), &maps.k1, bar,
+                          C::kChunks128K * (128 / C::kElem), hk, j * BN, u.b);
+            for (int c = 0; c < C::kVAtoms; ++c)
+              tma_load_4d(v_stage(st) + c * C::kVAtomBytes, &maps.v, bar, c * (C::kVAtomRow / C::kElem), hk,
+                          j * BN, u.b);
+          }
           ++kv_cnt;
         }
       }
       if (!ok) {
-        give_up();
+        if (leader) give_up();
         // every load already issued lands before the CTA may exit (its shared memory is released then)
         const int never = 0;
         const uint32_t ns = C::kStages;
@@ -347,115 +362,156 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // =========================== MMA issuer ===========================
     regs_dec<kRegsControl>();
-    if (lane == 0) {
+    {
+      const bool leader = elect_one();
       const uint32_t fmt = FP8 ? kFmtE4M3 : kFmtBF16;
       const uint32_t idesc_s = idesc_dense(fmt, fmt, false, false, kBlockM, BN);
+      // shared-memory descriptors of the first K step of each operand; a K step of 32 bytes moves the
+      // start address by 2 (16-byte units), a 128-byte chunk by rows * 8
+      const uint64_t q_desc0 = smem_desc(s_q, 16, 1024, kSwizzle128B);
+      const uint64_t q_tail0 = smem_desc(s_q + C::kChunks128K * (kBlockM * 128), 16, 512, kSwizzle64B);
+      const uint64_t k_desc0 = smem_desc(k_stage(0), 16, 1024, kSwizzle128B);
+      const uint64_t k_tail0 = smem_desc(k_stage(0) + C::kChunks128K * (BN * 128), 16, 512, kSwizzle64B);
+      constexpr uint32_t kQTile16 = C::kQTileBytes >> 4, kStage16 = C::kStageBytes >> 4;
       uint32_t kv_cnt = 0, s_seq = 0;
       uint32_t q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
       bool ok = true;
+      // the score tile issued last, while its reader has not yet been seen to copy it out
+      bool read_pending = false;
+      int last_t = 0, last_j = 0;
 
       // S = Q_t K^T for the K tile in stage st (both operands K-major in shared memory)
-      auto issue_s = [&](int t, int st) {
-        const uint32_t qa = s_q + t * C::kQTileBytes, kb = k_stage(st);
+      auto issue_s = [&](int t, uint32_t st) {
+        const uint64_t qd = q_desc0 + t * kQTile16, kd = k_desc0 + st * kStage16;
+        const uint64_t qt = q_tail0 + t * kQTile16, kt = k_tail0 + st * kStage16;
 #pragma unroll
         for (int ks = 0; ks < C::kKSteps; ++ks) {
           const int off = ks * 32;
           uint64_t ad, bd;
           if (off < C::kChunks128K * 128) {
-            ad = smem_desc(qa + (off / 128) * (kBlockM * 128) + (off % 128), 16, 1024, kSwizzle128B);
-            bd = smem_desc(kb + (off / 128) * (BN * 128) + (off % 128), 16, 1024, kSwizzle128B);
+            ad = qd + (off / 128) * (kBlockM * 8) + (off % 128) / 16;
+            bd = kd + (off / 128) * (BN * 8) + (off % 128) / 16;
           } else {
-            const int o2 = off - C::kChunks128K * 128;
-            ad = smem_desc(qa + C::kChunks128K * (kBlockM * 128) + o2, 16, 512, kSwizzle64B);
-            bd = smem_desc(kb + C::kChunks128K * (BN * 128) + o2, 16, 512, kSwizzle64B);
+            ad = qt + (off - C::kChunks128K * 128) / 16;
+            bd = kt + (off - C::kChunks128K * 128) / 16;
           }
-          if constexpr (FP8) mma_f8_ss(tmem + C::kColS, ad, bd, idesc_s, ks > 0);
-          else mma_f16_ss(tmem + C::kColS, ad, bd, idesc_s, ks > 0);
+          if (leader) {
+            if constexpr (FP8) mma_f8_ss(tmem + C::kColS, ad, bd, idesc_s, ks > 0);
+            else mma_f16_ss(tmem + C::kColS, ad, bd, idesc_s, ks > 0);
+          }
         }
-        tc_commit(smem_u32(&ctl.s_full[t]));
+        if (leader) tc_commit(smem_u32(&ctl.s_full[t]));
       };
       // O_t (| l_t) += P_t x [V | 1]
-      auto issue_pv = [&](int t, int st, bool first) {
+      auto issue_pv = [&](int t, uint32_t st, bool first) {
         const uint32_t o = tmem + C::col_o(t), pa = tmem + C::col_p(t), vb = v_stage(st);
         const uint32_t lbo = C::kOnes ? (s_ones - vb) : static_cast<uint32_t>(C::kVAtomBytes);
+        const uint64_t vd = C::kVAtomRow == 128 ? smem_desc(vb, lbo, 1024, kSwizzle128B)
+                                                : smem_desc(vb, lbo, 512, kSwizzle64B);
 #pragma unroll
         for (int ks = 0; ks < C::kPVSteps; ++ks) {
-          const uint32_t vaddr = vb + ks * C::kKeysPerStep * C::kVAtomRow;
-          const uint64_t vd = C::kVAtomRow == 128 ? smem_desc(vaddr, lbo, 1024, kSwizzle128B)
-                                                  : smem_desc(vaddr, lbo, 512, kSwizzle64B);
+          const uint64_t vdk = vd + (ks * C::kKeysPerStep * C::kVAtomRow) / 16;
           const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
-          if constexpr (FP8) {
-            // K step ks covers keys [32ks, 32ks+32): its e8m0 scale is byte ks of the scale word
-            mma_mxf8_ts(o, pa + ks * 8, vd, idesc_block_scaled(kFmtE4M3, kFmtE4M3, true, kBlockM, C::kNO, ks, 0),
-                        tmem + C::col_sfa(t), tmem + C::kColSFB, acc);
-          } else {
-            mma_f16_ts(o, pa + ks * 8, vd, idesc_dense(kFmtBF16, kFmtBF16, false, true, kBlockM, C::kNO), acc);
+          if (leader) {
+            if constexpr (FP8) {
+              // K step ks covers keys [32ks, 32ks+32): its e8m0 scale is byte ks of the scale word
+              mma_mxf8_ts(o, pa + ks * 8, vdk, idesc_block_scaled(kFmtE4M3, kFmtE4M3, true, kBlockM, C::kNO, ks, 0),
+                          tmem + C::col_sfa(t), tmem + C::kColSFB, acc);
+            } else {
+              mma_f16_ts(o, pa + ks * 8, vdk, idesc_dense(kFmtBF16, kFmtBF16, false, true, kBlockM, C::kNO), acc);
+            }
           }
         }
-        if (C::kSharedP) tc_commit(smem_u32(&ctl.p_free));
-      };
-      auto wait_kv = [&](uint32_t cnt) {
-        return mbar_wait(smem_u32(&ctl.kv_full[cnt % C::kStages]), (cnt / C::kStages) & 1, abort_flag, kWaitLimit);
-      };
-      // the shared S buffer: the s_seq-th score MMA waits until the previous score tile was read
-      auto wait_s_free = [&]() {
-        return s_seq == 0 || mbar_wait(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit);
-      };
-      auto wait_p = [&](int t) {
-        const bool r = mbar_wait(smem_u32(&ctl.p_full[t]), p_cnt[t] & 1, abort_flag, kWaitLimit);
-        ++p_cnt[t];
-        return r;
       };
 
       Unit u;
       for (int round = 0; ok && unit_at(p, round, u); ++round) {
-        const int n[2] = {tiles_for<BN>(p, u.r0, 0), tiles_for<BN>(p, u.r0, 1)};
-        const int nkv = n[1] > n[0] ? n[1] : n[0];
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (n[t] == 0) continue;
-          ok = mbar_wait(smem_u32(&ctl.q_full[t]), q_cnt[t] & 1, abort_flag, kWaitLimit);
-          ++q_cnt[t];
+        const int n0 = tiles_for<BN>(p, u.r0, 0), n1 = tiles_for<BN>(p, u.r0, 1);
+        const int nkv = n1 > n0 ? n1 : n0;
+        if (n0 > 0) {
+          ok = mbar_wait(smem_u32(&ctl.q_full[0]), q_cnt[0] & 1, abort_flag, kWaitLimit);
+          ++q_cnt[0];
+        }
+        if (ok && n1 > 0) {
+          ok = mbar_wait(smem_u32(&ctl.q_full[1]), q_cnt[1] & 1, abort_flag, kWaitLimit);
+          ++q_cnt[1];
         }
         if (!ok) break;
-        // order per K/V tile j: S0(j), PV1(j-1), S1(j), PV0(j); one extra pass for PV1(last)
-        for (int j = 0; j <= nkv && ok; ++j) {
-          const uint32_t cur = kv_cnt + j;
-          if (j < nkv && !(ok = wait_kv(cur))) break;
-          if (j < n[0]) {  // S0(j)
-            if (!(ok = wait_s_free())) break;
-            tc_fence_after();
-            issue_s(0, cur % C::kStages);
+
+        // PV_t(j).  Its completion is announced by pv_done only for the last two tiles of a query tile
+        // (the warpgroup learns of the others from its next score tile, issued after this PV).  A
+        // K/V stage is released after the later of its (at most two) PVs.
+        auto do_pv = [&](int t, int j) {
+          const int nt = t ? n1 : n0;
+          const uint32_t st = (kv_cnt + j) % C::kStages;
+          issue_pv(t, st, j == 0);
+          if (leader && j >= nt - 2) tc_commit(smem_u32(&ctl.pv_done[t]));
+          const bool pv0_last = n1 == 0 || (j == n0 - 1 && n1 > n0);
+          if (leader && (t == 0) == pv0_last) tc_commit(smem_u32(&ctl.kv_empty[st]));
+        };
+        // Waits until the last score tile issued has been copied out of the shared S buffer.  Its
+        // reader stored P of its previous tile before that, so the PV of that tile may follow; that
+        // tile is returned in rt / rj (rj < 0: nothing to unlock).
+        int rt = 0, rj = -1;
+        auto wait_read = [&]() -> bool {
+          rj = -1;
+          if (!read_pending) return true;
+          if (!mbar_wait(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit)) return false;
+          read_pending = false;
+          tc_fence_after();
+          if (last_j >= 1) {
+            rt = last_t;
+            rj = last_j - 1;
+          }
+          return true;
+        };
+
+        // score tiles in the order S0(0), S1(0), S0(1), S1(1), ...; each one waits until the previous
+        // was read, and the PV that read unlocks is issued next to it: after the score MMA when that
+        // belongs to the other query tile, before it when it belongs to the same one (so a score tile
+        // always follows the previous PV of its own query tile) or when the K/V ring is short
+        for (int j = 0; j < nkv && ok; ++j) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (j >= (t ? n1 : n0)) continue;
+            if (!(ok = wait_read())) break;
+            const bool pv_first = rj >= 0 && (rt == t || !C::kScoreFirst);
+            if (pv_first) do_pv(rt, rj);
+            if (t == 0 || j >= n0) {  // first score tile of K/V tile j
+              if (!(ok = mbar_wait(smem_u32(&ctl.kv_full[(kv_cnt + j) % C::kStages]),
+                                   ((kv_cnt + j) / C::kStages) & 1, abort_flag, kWaitLimit)))
+                break;
+              tc_fence_after();
+            }
+            issue_s(t, (kv_cnt + j) % C::kStages);
             ++s_seq;
-            if (j == n[0] - 1) tc_commit(smem_u32(&ctl.q_empty[0]));
+            read_pending = true;
+            last_t = t;
+            last_j = j;
+            if (leader && j == (t ? n1 : n0) - 1) tc_commit(smem_u32(&ctl.q_empty[t]));
+            if (rj >= 0 && !pv_first) do_pv(rt, rj);
           }
-          if (j >= 1 && j - 1 < n[1]) {  // PV1(j-1): the last use of K/V stage j-1
-            if (!(ok = wait_p(1))) break;
-            tc_fence_after();
-            issue_pv(1, (cur - 1) % C::kStages, j == 1);
-            tc_commit(smem_u32(&ctl.kv_empty[(cur - 1) % C::kStages]));
-            if (j == n[1]) tc_commit(smem_u32(&ctl.o_done[1]));
-          }
-          if (j < n[1]) {  // S1(j)
-            if (!(ok = wait_s_free())) break;
-            tc_fence_after();
-            issue_s(1, cur % C::kStages);
-            ++s_seq;
-            if (j == n[1] - 1) tc_commit(smem_u32(&ctl.q_empty[1]));
-          }
-          if (j < n[0]) {  // PV0(j)
-            if (!(ok = wait_p(0))) break;
-            tc_fence_after();
-            issue_pv(0, cur % C::kStages, j == 0);
-            if (j == n[0] - 1) tc_commit(smem_u32(&ctl.o_done[0]));
-            if (n[1] == 0) tc_commit(smem_u32(&ctl.kv_empty[cur % C::kStages]));
-          }
+        }
+        if (!ok) break;
+        // unit end: the read of the last score tile unlocks one more PV; the last PV of each query
+        // tile waits for the softmax warpgroup's P directly
+        if (!(ok = wait_read())) break;
+        if (rj >= 0) do_pv(rt, rj);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int nt = t ? n1 : n0;
+          if (nt == 0) continue;
+          if (!(ok = mbar_wait(smem_u32(&ctl.p_full[t]), p_cnt[t] & 1, abort_flag, kWaitLimit))) break;
+          ++p_cnt[t];
+          tc_fence_after();
+          do_pv(t, nt - 1);
         }
         kv_cnt += nkv;
       }
-      if (!ok) give_up();
-      // drain: all MMAs issued by this thread complete before TMEM is released
+      if (!ok && leader) give_up();
+      // drain: all MMAs issued by this warp complete before TMEM is released
       const int never = 0;
-      tc_commit(smem_u32(&ctl.drain));
+      if (leader) tc_commit(smem_u32(&ctl.drain));
       mbar_wait(smem_u32(&ctl.drain), 0, &never, kWaitLimit);
     }
   } else if (warp < 4) {
@@ -483,76 +539,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float a24 = a * 0x1p-24f;  // exact: scales Lean-P values into f16 subnormal units
     if constexpr (FP8) {
       if (t == 0) {
-        // e8m0 scale factors of V (all 1.0), written once; the first PV is issued only after this
-        // warpgroup's first p_full arrival, which releases these stores
+        // e8m0 scale factors of V (all 1.0), written once; every PV is issued after an arrival of
+        // this warpgroup (query tile 0 of a unit always has rows), which releases these stores
         tmem_st4(tmem + lane_addr + C::kColSFB, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
         tmem_st4(tmem + lane_addr + C::kColSFB + 4, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
         tmem_wait_st();
       }
     }
 
-    uint32_t s_cnt = 0, o_cnt = 0;
-    uint32_t pv_base = 0;  // BF16 shared P tile: PV MMAs of all earlier units
+    uint32_t s_cnt = 0;
+    uint32_t pv_ph = 0;  // pv_done phases of this query tile seen so far
     bool ok = true;
     Unit u;
     for (int round = 0; ok && unit_at(p, round, u); ++round) {
       const int n0 = tiles_for<BN>(p, u.r0, 0), n1 = tiles_for<BN>(p, u.r0, 1);
       const int ntiles = t == 0 ? n0 : n1;
-      if (ntiles == 0) {
-        pv_base += n0 + n1;
-        continue;
-      }
+      if (ntiles == 0) continue;
       const int row0 = u.r0 + t * kBlockM;  // first row of the tile
       const int row = row0 + rloc;
       const bool row_ok = row < p.S;
 
       int m_ref = 0;
       float l_bf16 = 0.0f;  // BF16: fp32 sum of the rounded probabilities of this row
-      for (int j = 0; j < ntiles; ++j) {
-        ok = mbar_wait(smem_u32(&ctl.s_full[t]), s_cnt & 1, abort_flag, kWaitLimit);
+      // Iteration j (0 <= j <= ntiles) first stores P of tile j-1, kept in registers: P_t and O_t are
+      // free once PV_t(j-2) completed, which the completion of score tile j certifies (it was issued
+      // after that PV); before the unit's last P the PV announces itself on pv_done.  Then it copies
+      // score tile j out of the shared S buffer and releases the buffer (that arrival also tells the
+      // MMA warp that P of tile j-1 is in place), and computes P of tile j.
+      constexpr int kNB = BN / kScaleBlock;
+      constexpr int kPW = BN * C::kElem / 4;  // 32-bit words of P per row
+      uint32_t pw[kPW];
+      uint32_t sfw = 0;
+      float lsum = 0.0f, f = 1.0f;
+      bool need = false;
+      for (int j = 0; j <= ntiles; ++j) {
+        const bool last = j == ntiles;
+        if (!last) {
+          ok = mbar_wait(smem_u32(&ctl.s_full[t]), s_cnt & 1, abort_flag, kWaitLimit);
+          ++s_cnt;
+        } else if (j > 1) {
+          ok = mbar_wait(smem_u32(&ctl.pv_done[t]), pv_ph & 1, abort_flag, kWaitLimit);
+          ++pv_ph;
+        }
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        ++s_cnt;
         tc_fence_after();
-        float s[BN];
-        {
-          uint32_t r[BN];
-#pragma unroll
-          for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
-          tmem_wait_ld();
-          tmem_ld_fence(r);
-#pragma unroll
-          for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r[i]);
-        }
-        // the scores are in registers: release the S buffer for the next score MMA
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl.s_free));
-
-        const int key0 = j * BN;
-        if (key0 + BN - 1 > row0) {  // tile touches the diagonal: mask keys after the row
-#pragma unroll
-          for (int i = 0; i < BN; ++i)
-            if (key0 + i > row) s[i] = -INFINITY;
-        }
-        constexpr int kNB = BN / kScaleBlock;
-        int e[kNB];
-        int e_top = kNoExp;
-#pragma unroll
-        for (int b = 0; b < kNB; ++b) {
-          // block exponent (FP8: ceil(max u / 8); BF16: ceil(max log2-score))
-          const float mx = max64(s + 64 * b);
-          const bool empty = mx == -INFINITY;
-          if constexpr (FP8) e[b] = empty ? kNoExp : static_cast<int>(ceilf(__fmul_rn(mx, a) * 0.125f));
-          else e[b] = empty ? kNoExp : static_cast<int>(ceilf(__fmul_rn(mx, a)));
-          e_top = max(e_top, e[b]);
-        }
-        if (j == 0) {
-          m_ref = e_top;  // key 0 is visible from every row, so e_top is finite
-        } else {
-          const bool need = e_top > m_ref + kRescaleBinades;
+        if (j > 0) {
           if (__any_sync(0xffffffffu, need)) {
-            // O_t is stable: the score MMA just received was issued after the previous PV of tile t
-            const float f = need ? exp2i(m_ref - e_top) : 1.0f;
 #pragma unroll
             for (int c = 0; c < DV / 32; ++c) {
               uint32_t r[32];
@@ -569,67 +601,91 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_wait_ld();
               tmem_ld_fence(lv);
               tmem_st1(tO + DV, __float_as_uint(__uint_as_float(lv[0]) * f));
-            } else {
-              l_bf16 *= f;
             }
-            if (need) m_ref = e_top;
           }
+          l_bf16 = l_bf16 * f + lsum;
+#pragma unroll
+          for (int c = 0; c < kPW / 16; ++c)
+            tmem_st16(tP + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pw + 16 * c));
+          if constexpr (FP8) tmem_st4(tmem + lane_addr + C::col_sfa(t), sfw, sfw, sfw, sfw);
         }
+        if (last) {
+          // the last P of the unit is announced directly (no later score read will imply it)
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl.p_full[t]));
+          break;
+        }
+        float s[BN];
+        {
+          uint32_t r[BN];
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+          tmem_wait_ld();
+          tmem_ld_fence(r);
+#pragma unroll
+          for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r[i]);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl.s_free));
 
+        const int key0 = j * BN;
+        if (key0 + BN - 1 > row0) {  // tile touches the diagonal: mask keys after the row
+#pragma unroll
+          for (int i = 0; i < BN; ++i)
+            if (key0 + i > row) s[i] = -INFINITY;
+        }
+        int e[kNB];
+        int e_top = kNoExp;
+#pragma unroll
+        for (int b = 0; b < kNB; ++b) {
+          // block exponent (FP8: ceil(max u / 8); BF16: ceil(max log2-score))
+          const float mx = max64(s + 64 * b);
+          const bool empty = mx == -INFINITY;
+          if constexpr (FP8) e[b] = empty ? kNoExp : static_cast<int>(ceilf(__fmul_rn(mx, a) * 0.125f));
+          else e[b] = empty ? kNoExp : static_cast<int>(ceilf(__fmul_rn(mx, a)));
+          e_top = max(e_top, e[b]);
+        }
+        // integer reference exponent: set by the first tile (key 0 is visible from every row, so
+        // e_top is finite there), raised lazily when a block exceeds it by more than the threshold
+        need = j > 0 && e_top > m_ref + kRescaleBinades;
+        f = need ? exp2i(m_ref - e_top) : 1.0f;  // rescale of the earlier O and l
+        if (j == 0 || need) m_ref = e_top;
+
+        // P of this tile, in registers, relative to the (new) reference
+        sfw = 0;
+        lsum = 0.0f;
         if constexpr (FP8) {
-          uint32_t sfw = 0;
 #pragma unroll
           for (int b = 0; b < kNB; ++b) {
             const int eb = e[b] == kNoExp ? m_ref : e[b];
-            uint32_t pw[16];
-            leanp_block(s + 64 * b, a24, eb, pw);
-            tmem_st16(tP + 16 * b, pw);
+            leanp_block(s + 64 * b, a24, eb, *reinterpret_cast<uint32_t(*)[16]>(pw + 16 * b));
             int sf = 127 + eb - m_ref;
             sf = sf < 0 ? 0 : (sf > 254 ? 254 : sf);
             // two 32-key MMA steps per 64-key block: bytes 2b and 2b+1 of the scale word
             sfw |= static_cast<uint32_t>(sf) * (0x0101u << (16 * b));
           }
           if (kNB == 1) sfw |= sfw << 16;
-          tmem_st4(tmem + lane_addr + C::col_sfa(t), sfw, sfw, sfw, sfw);
         } else {
-          if constexpr (C::kSharedP) {
-            // the shared P tile is free once the PV just before this one (in issue order) completed:
-            // per unit the PV order is PV0(0), PV1(0), PV0(1), PV1(1), ..., then PV1 of the tail tiles
-            // (a unit whose second tile is empty issues PV0(0), PV0(1), ...)
-            const uint32_t k = pv_base + (n1 == 0 ? j : (j < n0 ? 2 * j + t : n0 + j));
-            if (k > 0) {
-              ok = mbar_wait(smem_u32(&ctl.p_free), (k - 1) & 1, abort_flag, kWaitLimit);
-              if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            }
-            tc_fence_after();
-          }
           const float negm = -static_cast<float>(m_ref);
           float lacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t pw[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int k2 = 32 * c + 2 * i;
-              pw[i] = cvt_bf16x2(ex2(__fmaf_rn(s[k2 + 1], a, negm)), ex2(__fmaf_rn(s[k2], a, negm)));
-              lacc[i & 3] += __uint_as_float(pw[i] << 16) + __uint_as_float(pw[i] & 0xFFFF0000u);
-            }
-            tmem_st16(tP + 16 * c, pw);
+          for (int i = 0; i < kPW; ++i) {
+            pw[i] = cvt_bf16x2(ex2(__fmaf_rn(s[2 * i + 1], a, negm)), ex2(__fmaf_rn(s[2 * i], a, negm)));
+            lacc[i & 3] += __uint_as_float(pw[i] << 16) + __uint_as_float(pw[i] & 0xFFFF0000u);
           }
-          l_bf16 += (lacc[0] + lacc[1]) + (lacc[2] + lacc[3]);
+          lsum = (lacc[0] + lacc[1]) + (lacc[2] + lacc[3]);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl.p_full[t]));
       }
       if (!ok) break;
-      pv_base += n0 + n1;
 
-      // epilogue: out = O * (dv / l) -> bf16
-      ok = mbar_wait(smem_u32(&ctl.o_done[t]), o_cnt & 1, abort_flag, kWaitLimit);
+      // epilogue: out = O * (dv / l) -> bf16, once the last PV of this tile completed
+      ok = mbar_wait(smem_u32(&ctl.pv_done[t]), pv_ph & 1, abort_flag, kWaitLimit);
+      ++pv_ph;
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      ++o_cnt;
       tc_fence_after();
       float l;
       if constexpr (FP8) {
