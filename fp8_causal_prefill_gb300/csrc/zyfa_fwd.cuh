@@ -27,9 +27,10 @@
 // the warpgroup's previous P is in TMEM, so PV_t(j-1) is issued right after the score MMA that follows
 // the read of S_t(j): score MMAs never wait for a softmax computation, and the PV of one tile keeps
 // the tensor core busy while the other tile's scores are handed over (the pages' ping-pong, here
-// between two query tiles with mbarrier completion tracking).  A warpgroup may rescale O_t or
-// overwrite P_t once the previous PV of its tile completed: the completion of its next score tile,
-// issued after that PV, certifies it; the last two PVs of a query tile also commit to pv_done.
+// between two query tiles with mbarrier completion tracking).  Every PV commits to its tile's
+// pv_done barrier; a warpgroup stores P_t(j) (and rescales O_t) once PV_t(j-1) has completed.
+// The MMA warp's own instruction stream is on the critical path, so the middle of every unit (both
+// query tiles active) runs as a fixed, branch-free sequence.
 // Every tcgen05 instruction costs the issuing thread tens of cycles, so score MMAs are 128 keys wide.
 //
 // Tensor memory (512 columns x 128 lanes; lane = query row of a tile):
@@ -230,6 +231,28 @@ __device__ __forceinline__ void leanp_block(const float* s, float a24, int e, ui
     const float t2 = __fmaf_rn(s[4 * i + 2], a24, c24);
     const float t3 = __fmaf_rn(s[4 * i + 3], a24, c24);
     pw[i] = prmt(cvt_relu_f16x2(t1, t0), cvt_relu_f16x2(t3, t2), 0x6420u);
+  }
+}
+
+template <bool FP8, int DV>
+__device__ __forceinline__ void rescale_o(uint32_t tO, float f) {
+  using namespace ptx;
+#pragma unroll
+  for (int c = 0; c < DV / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(tO + 32 * c, r);
+    tmem_wait_ld();
+    tmem_ld_fence(r);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+    tmem_st32(tO + 32 * c, r);
+  }
+  if constexpr (FP8) {
+    uint32_t lv[1];
+    tmem_ld1(tO + DV, lv[0]);
+    tmem_wait_ld();
+    tmem_ld_fence(lv);
+    tmem_st1(tO + DV, __float_as_uint(__uint_as_float(lv[0]) * f));
   }
 }
 
@@ -438,14 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
 
-        // PV_t(j).  Its completion is announced by pv_done only for the last two tiles of a query tile
-        // (the warpgroup learns of the others from its next score tile, issued after this PV).  A
-        // K/V stage is released after the later of its (at most two) PVs.
+        // PV_t(j), announced on pv_done.  A K/V stage is released after the later of its (at most
+        // two) PVs.
         auto do_pv = [&](int t, int j) {
           const int nt = t ? n1 : n0;
           const uint32_t st = (kv_cnt + j) % C::kStages;
           issue_pv(t, st, j == 0);
-          if (leader && j >= nt - 2) tc_commit(smem_u32(&ctl.pv_done[t]));
+          if (leader) tc_commit(smem_u32(&ctl.pv_done[t]));
           const bool pv0_last = n1 == 0 || (j == n0 - 1 && n1 > n0);
           if (leader && (t == 0) == pv0_last) tc_commit(smem_u32(&ctl.kv_empty[st]));
         };
@@ -471,6 +493,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         // belongs to the other query tile, before it when it belongs to the same one (so a score tile
         // always follows the previous PV of its own query tile) or when the K/V ring is short
         for (int j = 0; j < nkv && ok; ++j) {
+          if (C::kScoreFirst && j >= 1 && j < n0 && n1 > 0) {
+            // steady state (both query tiles active): S0(j), PV1(j-2), S1(j), PV0(j-1)
+            const uint32_t st = (kv_cnt + j) % C::kStages;
+            if (!(ok = mbar_wait(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit))) break;
+            if (!(ok = mbar_wait(smem_u32(&ctl.kv_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag,
+                                 kWaitLimit)))
+              break;
+            tc_fence_after();
+            issue_s(0, st);
+            if (leader && j == n0 - 1) tc_commit(smem_u32(&ctl.q_empty[0]));
+            if (j >= 2) {
+              const uint32_t st2 = (kv_cnt + j - 2) % C::kStages;
+              issue_pv(1, st2, j == 2);
+              if (leader) {
+                tc_commit(smem_u32(&ctl.pv_done[1]));
+                tc_commit(smem_u32(&ctl.kv_empty[st2]));
+              }
+            }
+            if (!(ok = mbar_wait(smem_u32(&ctl.s_free), s_seq & 1, abort_flag, kWaitLimit))) break;
+            tc_fence_after();
+            issue_s(1, st);
+            const uint32_t st1 = (kv_cnt + j - 1) % C::kStages;
+            issue_pv(0, st1, j == 1);
+            if (leader) tc_commit(smem_u32(&ctl.pv_done[0]));
+            s_seq += 2;
+            last_t = 1;
+            last_j = j;
+            read_pending = true;
+            continue;
+          }
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (j >= (t ? n1 : n0)) continue;
@@ -561,62 +613,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       int m_ref = 0;
       float l_bf16 = 0.0f;  // BF16: fp32 sum of the rounded probabilities of this row
-      // Iteration j (0 <= j <= ntiles) first stores P of tile j-1, kept in registers: P_t and O_t are
-      // free once PV_t(j-2) completed, which the completion of score tile j certifies (it was issued
-      // after that PV); before the unit's last P the PV announces itself on pv_done.  Then it copies
-      // score tile j out of the shared S buffer and releases the buffer (that arrival also tells the
-      // MMA warp that P of tile j-1 is in place), and computes P of tile j.
+      // Iteration j copies score tile j out of the shared S buffer and releases it (the release also
+      // tells the MMA warp that P of tile j-1, stored before, is in place), computes P of tile j and
+      // stores it as soon as PV_t(j-1), which reads the same TMEM buffer, has completed (pv_done).
       constexpr int kNB = BN / kScaleBlock;
       constexpr int kPW = BN * C::kElem / 4;  // 32-bit words of P per row
-      uint32_t pw[kPW];
-      uint32_t sfw = 0;
-      float lsum = 0.0f, f = 1.0f;
-      bool need = false;
-      for (int j = 0; j <= ntiles; ++j) {
-        const bool last = j == ntiles;
-        if (!last) {
-          ok = mbar_wait(smem_u32(&ctl.s_full[t]), s_cnt & 1, abort_flag, kWaitLimit);
-          ++s_cnt;
-        } else if (j > 1) {
-          ok = mbar_wait(smem_u32(&ctl.pv_done[t]), pv_ph & 1, abort_flag, kWaitLimit);
-          ++pv_ph;
-        }
+      for (int j = 0; j < ntiles; ++j) {
+        ok = mbar_wait(smem_u32(&ctl.s_full[t]), s_cnt & 1, abort_flag, kWaitLimit);
+        ++s_cnt;
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        if (j > 0) {
-          if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-            for (int c = 0; c < DV / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(tO + 32 * c, r);
-              tmem_wait_ld();
-              tmem_ld_fence(r);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-              tmem_st32(tO + 32 * c, r);
-            }
-            if constexpr (FP8) {
-              uint32_t lv[1];
-              tmem_ld1(tO + DV, lv[0]);
-              tmem_wait_ld();
-              tmem_ld_fence(lv);
-              tmem_st1(tO + DV, __float_as_uint(__uint_as_float(lv[0]) * f));
-            }
-          }
-          l_bf16 = l_bf16 * f + lsum;
-#pragma unroll
-          for (int c = 0; c < kPW / 16; ++c)
-            tmem_st16(tP + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pw + 16 * c));
-          if constexpr (FP8) tmem_st4(tmem + lane_addr + C::col_sfa(t), sfw, sfw, sfw, sfw);
-        }
-        if (last) {
-          // the last P of the unit is announced directly (no later score read will imply it)
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctl.p_full[t]));
-          break;
-        }
         float s[BN];
         {
           uint32_t r[BN];
@@ -649,15 +655,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           else e[b] = empty ? kNoExp : static_cast<int>(ceilf(__fmul_rn(mx, a)));
           e_top = max(e_top, e[b]);
         }
-        // integer reference exponent: set by the first tile (key 0 is visible from every row, so
-        // e_top is finite there), raised lazily when a block exceeds it by more than the threshold
-        need = j > 0 && e_top > m_ref + kRescaleBinades;
-        f = need ? exp2i(m_ref - e_top) : 1.0f;  // rescale of the earlier O and l
+        const bool need = j > 0 && e_top > m_ref + kRescaleBinades;
+        const float f = need ? exp2i(m_ref - e_top) : 1.0f;
         if (j == 0 || need) m_ref = e_top;
 
-        // P of this tile, in registers, relative to the (new) reference
-        sfw = 0;
-        lsum = 0.0f;
+        uint32_t pw[kPW];
+        uint32_t sfw = 0;
+        float lsum = 0.0f;
         if constexpr (FP8) {
 #pragma unroll
           for (int b = 0; b < kNB; ++b) {
@@ -665,7 +669,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             leanp_block(s + 64 * b, a24, eb, *reinterpret_cast<uint32_t(*)[16]>(pw + 16 * b));
             int sf = 127 + eb - m_ref;
             sf = sf < 0 ? 0 : (sf > 254 ? 254 : sf);
-            // two 32-key MMA steps per 64-key block: bytes 2b and 2b+1 of the scale word
             sfw |= static_cast<uint32_t>(sf) * (0x0101u << (16 * b));
           }
           if (kNB == 1) sfw |= sfw << 16;
@@ -678,6 +681,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             lacc[i & 3] += __uint_as_float(pw[i] << 16) + __uint_as_float(pw[i] & 0xFFFF0000u);
           }
           lsum = (lacc[0] + lacc[1]) + (lacc[2] + lacc[3]);
+        }
+        if (j > 0) {
+          ok = mbar_wait(smem_u32(&ctl.pv_done[t]), pv_ph & 1, abort_flag, kWaitLimit);
+          ++pv_ph;
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) rescale_o<FP8, DV>(tO, f);
+        }
+        l_bf16 = l_bf16 * f + lsum;
+#pragma unroll
+        for (int c = 0; c < kPW / 16; ++c) tmem_st16(tP + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pw + 16 * c));
+        if constexpr (FP8) tmem_st4(tmem + lane_addr + C::col_sfa(t), sfw, sfw, sfw, sfw);
+        if (j + 1 == ntiles) {
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl.p_full[t]));
         }
       }
       if (!ok) break;
