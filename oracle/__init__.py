@@ -12,6 +12,9 @@ Functions and the passages they follow (page title, section):
 * ``exact_causal_attention`` (O1): causal softmax attention, float64 (ZYFA abstract, first sentences).
 * ``leanp_causal_attention`` (O2): Lean P, per-64-key power-of-two scaling, rounded-row-sum
   normalisation (ZYFA abstract, techniques (1) and (3); "Три приёма"; "Tiga Trik").
+* ``exactp_causal_attention`` (O2x): O2 with exact exponentiation and e4m3 rounding in place of Lean P,
+  the baseline the pages compare Lean P with ("Tiga Trik": 5.9% vs 7.5% per probability).
+* ``return_lse=True`` on O1, O2, O2x, O4: ln sum_j exp(s_ij) per row (flash_attn_func's softmax_lse).
 * ``plain_fp8_causal_attention`` (O3): exact-exponential FP8 softmax, comparison only.
 * ``bf16_causal_attention`` (O4): the BF16 twin (the pages give no BF16 numerics; plainest reading).
 """
@@ -19,5 +22,6 @@ from .formats import (E4M3_MAX, bf16_bits_to_float, bf16_round, e4m3_decode,  # 
                       e4m3_encode_rne_satfinite, fl32)
 from .attention import (LEANP_C0, SCALE_BLOCK, bf16_causal_attention,  # noqa: F401
                         bf16_round_f64, bf16_score_scale, default_softmax_scale, dequant_e4m3,
-                        exact_causal_attention, fp8_score_scale, leanp_causal_attention, leanp_code,
+                        exact_causal_attention, exactp_causal_attention, exactp_code, fp8_score_scale,
+                        leanp_causal_attention, leanp_code,
                         leanp_row_weights, plain_fp8_causal_attention, rel_l2)

@@ -34,6 +34,18 @@ may be evaluated; the row loop is chunked only to bound memory and does not chan
   [-6, 0] to the exact code of 2^x, 8x + 56.  Blocks whose exponent lies more than 126 binades below
   the row's largest block exponent get weight 0 (their scale leaves the e8m0 range).
 
+* ``exactp_causal_attention`` (O2x): O2 with step 4 replaced by exact exponentiation and rounding,
+  ``code = rne_e4m3(2^fl32(S32*a/8 - e))``: the "exact P" the pages measure Lean P against (its
+  per-probability error is that of e4m3 rounding, 5.9%, against Lean P's 7.5%; and it needs an
+  exponential per probability, the vector work Lean P removes).  Block exponents and the rounded-sum
+  normalisation are those of O2.
+
+* Log-sum-exp (``return_lse=True`` on O1, O2, O2x and O4): ``lse_i = ln sum_j exp(s_ij)`` with
+  ``s_ij`` the real (descaled) score.  For O1 it is computed in float64 from the exact scores; for the
+  block-scaled paths it is ``ln sum_j dec(code_ij) 2^e_b`` (the rounded weights carry the
+  probabilities' scale), for O4 ``ln sum_j p_j + M ln 2``.  flash_attn_func returns the same
+  quantity (softmax_lse, natural logarithm) beside the output.
+
 * ``plain_fp8_causal_attention`` (O3): the usual FP8 softmax, for comparison only: exact
   probabilities relative to the row max, rounded to e4m3 once, divided by the unrounded sum.
 
@@ -111,7 +123,14 @@ def leanp_row_weights(s32, a: float, c0: float = LEANP_C0, block: int = SCALE_BL
     return _leanp_weights(s32, valid, a, c0, block)
 
 
-def _leanp_weights(s32, valid, a, c0, block):
+def exactp_code(t_exact) -> np.ndarray:
+    """Exact-P code from the exact value ``S32*a/8 - e``: one fp32 rounding (as a fused multiply-add
+    produces), then 2^t rounded to nearest e4m3 (ties to even), as O2x's step 4."""
+    t = fl32(t_exact)
+    return e4m3_encode_rne_satfinite(np.exp2(t)).astype(np.int64)
+
+
+def _leanp_weights(s32, valid, a, c0, block, exact=False):
     r, n = s32.shape
     nb = -(-n // block)
     pad = nb * block - n
@@ -122,7 +141,10 @@ def _leanp_weights(s32, valid, a, c0, block):
         e = np.ceil(u_max * 0.125)
     e_key = np.repeat(e, block, axis=1)[:, :n]
     e_safe = np.where(np.isfinite(e_key), e_key, 0.0)
-    code = leanp_code(s32 * a + (c0 - 8.0 * e_safe))
+    if exact:
+        code = exactp_code(np.where(valid, s32 * (a / 8.0) - e_safe, -np.inf))
+    else:
+        code = leanp_code(s32 * a + (c0 - 8.0 * e_safe))
     code = np.where(valid, code, 0)
     e_max = np.max(np.where(np.isfinite(e), e, -np.inf), axis=1, keepdims=True)
     rel = e_safe - e_max
@@ -143,8 +165,9 @@ def _causal_mask(row_idx, n_keys):
     return np.arange(n_keys)[None, :] <= row_idx[:, None]
 
 
-def exact_causal_attention(q, k, v, softmax_scale, rows=None, heads=None) -> np.ndarray:
-    """O1: float64 causal attention on real-valued (dequantised) inputs."""
+def exact_causal_attention(q, k, v, softmax_scale, rows=None, heads=None, return_lse=False):
+    """O1: float64 causal attention on real-valued (dequantised) inputs (and, with ``return_lse``,
+    ln sum_j exp(s_ij) per row, [B, R, len(heads)])."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -153,6 +176,7 @@ def exact_causal_attention(q, k, v, softmax_scale, rows=None, heads=None) -> np.
     rows = _rows(s_, rows)
     hs = _heads(h_, heads)
     out = np.zeros((b_, len(rows), len(hs), dv))
+    lse = np.zeros((b_, len(rows), len(hs)))
     for b in range(b_):
         for oi, h in enumerate(hs):
             kh = h // (h_ // hkv)
@@ -163,9 +187,11 @@ def exact_causal_attention(q, k, v, softmax_scale, rows=None, heads=None) -> np.
                 s = softmax_scale * (q[b, ri, h, :] @ kk[:n].T)
                 mask = _causal_mask(ri, n)
                 s = np.where(mask, s, -np.inf)
-                p = np.exp(s - s.max(axis=1, keepdims=True))
+                mx = s.max(axis=1, keepdims=True)
+                p = np.exp(s - mx)
                 out[b, c:c + len(ri), oi, :] = (p @ vv[:n]) / p.sum(axis=1, keepdims=True)
-    return out
+                lse[b, c:c + len(ri), oi] = mx[:, 0] + np.log(p.sum(axis=1))
+    return (out, lse) if return_lse else out
 
 
 def dequant_e4m3(x8, descale: float) -> np.ndarray:
@@ -174,14 +200,17 @@ def dequant_e4m3(x8, descale: float) -> np.ndarray:
 
 
 def leanp_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=None, heads=None,
-                           c0: float = LEANP_C0, return_codes: bool = False):
-    """O2: Lean P + per-64-key power-of-two block scaling + rounded-row-sum normalisation."""
+                           c0: float = LEANP_C0, return_codes: bool = False, return_lse: bool = False,
+                           exact: bool = False):
+    """O2: Lean P + per-64-key power-of-two block scaling + rounded-row-sum normalisation.
+    ``exact=True`` gives O2x (exact exponentiation and rounding in place of Lean P)."""
     a = fp8_score_scale(softmax_scale, dq, dk)
     b_, s_, h_, _ = q8.shape
     hkv, dvd = k8.shape[2], v8.shape[3]
     rows = _rows(s_, rows)
     hs = _heads(h_, heads)
     out = np.zeros((b_, len(rows), len(hs), dvd))
+    lse = np.zeros((b_, len(rows), len(hs)))
     codes_out = {}
     n_keys = int(rows.max()) + 1 if len(rows) else 0
     for b in range(b_):
@@ -193,11 +222,26 @@ def leanp_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=None, hea
                 ri = rows[c:c + _ROW_CHUNK]
                 n = int(ri.max()) + 1 if len(ri) else 0
                 s32 = fl32(qh[ri] @ kk[:n].T)
-                code, _, w = _leanp_weights(s32, _causal_mask(ri, n), a, c0, SCALE_BLOCK)
+                code, e, w = _leanp_weights(s32, _causal_mask(ri, n), a, c0, SCALE_BLOCK, exact=exact)
                 out[b, c:c + len(ri), oi, :] = float(dv) * (w @ vv[:n]) / w.sum(axis=1, keepdims=True)
+                if return_lse:
+                    e_max = np.max(np.where(np.isfinite(e), e, -np.inf), axis=1)
+                    lse[b, c:c + len(ri), oi] = np.log(w.sum(axis=1)) + e_max * math.log(2.0)
                 if return_codes:
                     codes_out[(b, h, c)] = code
-    return (out, codes_out) if return_codes else out
+    res = (out,)
+    if return_codes:
+        res += (codes_out,)
+    if return_lse:
+        res += (lse,)
+    return res[0] if len(res) == 1 else res
+
+
+def exactp_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=None, heads=None,
+                            return_lse: bool = False):
+    """O2x: O2 with exact exponentiation and rounding of each probability in place of Lean P."""
+    return leanp_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=rows, heads=heads,
+                                  return_lse=return_lse, exact=True)
 
 
 def plain_fp8_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=None, heads=None):
@@ -225,7 +269,7 @@ def plain_fp8_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=None,
     return out
 
 
-def bf16_causal_attention(qb, kb, vb, softmax_scale, rows=None, heads=None):
+def bf16_causal_attention(qb, kb, vb, softmax_scale, rows=None, heads=None, return_lse=False):
     """O4: the BF16 twin on bf16-valued inputs (float64 arrays holding bf16 values)."""
     qb = np.asarray(qb, dtype=np.float64)
     kb = np.asarray(kb, dtype=np.float64)
@@ -236,6 +280,7 @@ def bf16_causal_attention(qb, kb, vb, softmax_scale, rows=None, heads=None):
     rows = _rows(s_, rows)
     hs = _heads(h_, heads)
     out = np.zeros((b_, len(rows), len(hs), dvd))
+    lse = np.zeros((b_, len(rows), len(hs)))
     for b in range(b_):
         for oi, h in enumerate(hs):
             kh = h // (h_ // hkv)
@@ -250,7 +295,8 @@ def bf16_causal_attention(qb, kb, vb, softmax_scale, rows=None, heads=None):
                 t = fl32(s32 * a2 - m)
                 p = np.where(mask, bf16_round_f64(np.exp2(np.where(mask, t, 0.0))), 0.0)
                 out[b, c:c + len(ri), oi, :] = (p @ vv[:n]) / p.sum(axis=1, keepdims=True)
-    return out
+                lse[b, c:c + len(ri), oi] = np.log(p.sum(axis=1)) + m[:, 0] * math.log(2.0)
+    return (out, lse) if return_lse else out
 
 
 def rel_l2(x, ref) -> float:

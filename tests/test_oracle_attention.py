@@ -312,3 +312,106 @@ def test_sample_rows_cover_edges():
     r = sample_rows(32768)
     assert r[0] == 0 and r[-1] == 32767 and len(r) == 128 * 2 + 512
     assert np.all(np.diff(r) > 0)
+
+
+# ----------------------------------------------------------------------------------------------
+# Exact P (the comparison the pages make for Lean P) and log-sum-exp
+
+
+@pytest.mark.parametrize("x,code,value", [(int(a), int(b), float(c)) for a, b, c in
+                                          _read_table("leanp_integer_x.txt")])
+def test_exactp_integer_powers_match_leanp(x, code, value):
+    # At whole binades both forms give the exact e4m3 code of 2^x (8x + 56).
+    assert int(O.exactp_code(np.array([float(x)]))[0]) == code
+
+
+def test_exactp_error_is_the_pages_exact_rounding_figure():
+    t = np.linspace(-6.0, 0.0, 600001)
+    code = O.exactp_code(t)
+    err = np.abs(O.e4m3_decode(code.astype(np.uint8)) - 2.0 ** t) / 2.0 ** t
+    assert err.max() <= PAGE["exact_rounding_max_rel_error"]
+    assert abs(err.max() - 1.0 / 17.0) < 1e-4
+    # and it never does worse than Lean P on the same grid
+    lean = _leanp_rel_error(O.LEANP_C0, t)
+    assert err.max() < lean.max()
+
+
+def test_exactp_reduces_to_exact_softmax_on_integer_scores():
+    # Same construction as the Lean-P case: integer base-2 scores make every probability an exact
+    # power of two, so exact P, Lean P and softmax in base 2 coincide.
+    rng = np.random.default_rng(6)
+    b, s, h, hkv, dqk, dv = 1, 200, 4, 2, 32, 8
+    qv = np.zeros((b, s, h, dqk))
+    idx = rng.integers(0, dqk, (b, s, h))
+    np.put_along_axis(qv, idx[..., None], 1.0, axis=3)
+    top = np.repeat(rng.integers(0, 4, (b, -(-s // 64), hkv)), 64, axis=1)[:, :s]
+    kv = np.floor(rng.uniform(0, 1, (b, s, hkv, dqk)) * (top[..., None] + 1))
+    vv = O.e4m3_decode(O.e4m3_encode_rne_satfinite(rng.standard_normal((b, s, hkv, dv))))
+    q8, k8, v8 = _problem_from_values(qv, kv, vv)
+    dk = _eight_over_l8()
+    ox = O.exactp_causal_attention(q8, k8, v8, 1.0, dk, 1.0, 1.0)
+    o2 = O.leanp_causal_attention(q8, k8, v8, 1.0, dk, 1.0, 1.0)
+    np.testing.assert_array_equal(ox, o2)
+    raw = torch.einsum("bshd,bthd->bhst", torch.from_numpy(qv),
+                       torch.from_numpy(kv).repeat_interleave(h // hkv, dim=2))
+    mask = torch.ones(s, s, dtype=torch.bool).tril()
+    p = torch.softmax(torch.where(mask, raw * math.log(2.0), torch.tensor(-math.inf, dtype=raw.dtype)), -1)
+    ref = torch.einsum("bhst,bthd->bshd", p, torch.from_numpy(vv).repeat_interleave(h // hkv, dim=2))
+    np.testing.assert_allclose(ox, ref.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_exactp_normalises_by_its_rounded_sum_and_differs_from_leanp():
+    p = make_problem(Shape(1, 300, 2, 1, 64, 16), seed=8, bf16=False)
+    ones = np.full((1, 300, 1, 16), 0x38, dtype=np.uint8)
+    out = O.exactp_causal_attention(p.q8.numpy(), p.k8.numpy(), ones, p.dq, p.dk, 1.0, 0.125)
+    assert np.max(np.abs(out - 1.0)) < 1e-15
+    args = (p.q8.numpy(), p.k8.numpy(), p.v8.numpy(), p.dq, p.dk, p.dv, 0.125)
+    assert O.rel_l2(O.exactp_causal_attention(*args), O.leanp_causal_attention(*args)) > 1e-3
+
+
+def test_lse_of_exact_attention_matches_torch_logsumexp():
+    rng = np.random.default_rng(13)
+    b, s, h, hkv, d = 2, 45, 4, 2, 16
+    q = rng.standard_normal((b, s, h, d))
+    k = rng.standard_normal((b, s, hkv, d))
+    v = rng.standard_normal((b, s, hkv, d))
+    _, lse = O.exact_causal_attention(q, k, v, 0.4, return_lse=True)
+    kt = torch.from_numpy(k).repeat_interleave(h // hkv, dim=2)
+    sc = 0.4 * torch.einsum("bshd,bthd->bhst", torch.from_numpy(q), kt)
+    sc = torch.where(torch.ones(s, s, dtype=torch.bool).tril(), sc, torch.tensor(-math.inf, dtype=sc.dtype))
+    ref = torch.logsumexp(sc, dim=-1).permute(0, 2, 1).numpy()        # [B, S, H]
+    np.testing.assert_allclose(lse, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_lse_of_zero_queries_is_log_of_row_length_on_every_path():
+    # Q = 0: every visible score is 0, so lse_i = ln(i + 1) exactly (closed form).
+    rng = np.random.default_rng(14)
+    s = 130
+    q8 = np.zeros((1, s, 2, 16), dtype=np.uint8)
+    k8 = O.e4m3_encode_rne_satfinite(rng.standard_normal((1, s, 1, 16)))
+    v8 = O.e4m3_encode_rne_satfinite(rng.standard_normal((1, s, 1, 8)))
+    expect = np.log(np.arange(1, s + 1))[None, :, None]
+    for f in (O.leanp_causal_attention, O.exactp_causal_attention):
+        _, lse = f(q8, k8, v8, 0.5, 0.5, 1.0, 0.125, return_lse=True)
+        np.testing.assert_allclose(lse, np.repeat(expect, 2, axis=2), rtol=0, atol=1e-13)
+    _, lse1 = O.exact_causal_attention(np.zeros((1, s, 2, 16)), O.e4m3_decode(k8), O.e4m3_decode(v8), 0.125,
+                                       return_lse=True)
+    np.testing.assert_allclose(lse1, np.repeat(expect, 2, axis=2), rtol=0, atol=1e-13)
+    _, lse4 = O.bf16_causal_attention(np.zeros((1, s, 2, 16)), O.e4m3_decode(k8), O.e4m3_decode(v8), 0.125,
+                                      return_lse=True)
+    np.testing.assert_allclose(lse4, np.repeat(expect, 2, axis=2), rtol=0, atol=1e-13)
+
+
+def test_lse_of_block_scaled_paths_within_rounding_bounds_of_exact():
+    # Each rounded weight is within the per-probability error bound delta of the true value, so the
+    # log of their sum is within -ln(1 - delta) of the exact log-sum-exp.
+    p = make_problem(Shape(1, 400, 2, 1, 64, 16), seed=15, bf16=False)
+    sc = 0.125
+    args = (p.q8.numpy(), p.k8.numpy(), p.v8.numpy(), p.dq, p.dk, p.dv, sc)
+    q, k, v = (O.dequant_e4m3(t.numpy(), d) for t, d in ((p.q8, p.dq), (p.k8, p.dk), (p.v8, p.dv)))
+    _, l1 = O.exact_causal_attention(q, k, v, sc, return_lse=True)
+    _, l2 = O.leanp_causal_attention(*args, return_lse=True)
+    _, lx = O.exactp_causal_attention(*args, return_lse=True)
+    assert np.max(np.abs(l2 - l1)) <= -math.log1p(-PAGE["leanp_max_rel_error"])
+    assert np.max(np.abs(lx - l1)) <= -math.log1p(-PAGE["exact_rounding_max_rel_error"])
+    assert np.max(np.abs(l2 - l1)) > 1e-4          # the rounding is visible, not skipped
