@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--dtype", choices=["fp8", "bf16"], default="fp8")
     ap.add_argument("--config", default="bench32k")
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling a smaller case)")
+    ap.add_argument("--p-mode", choices=["lean", "exact"], default="lean",
+                    help="FP8 probabilities: Lean P (the method) or exact exponential (the ablation)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
@@ -75,9 +77,10 @@ def shape_for(args):
     return sh
 
 
-def workload_name(sh, dtype):
+def workload_name(sh, dtype, p_mode="lean"):
+    extra = ", exact-P ablation" if (dtype == "fp8" and p_mode == "exact") else ""
     return (f"{'e4m3' if dtype == 'fp8' else 'bf16'} causal prefill B={sh.B} H={sh.H} H_kv={sh.H_kv} S={sh.S} "
-            f"D_qk={sh.D_qk} D_v={sh.D_v} {sh.kind} inputs")
+            f"D_qk={sh.D_qk} D_v={sh.D_v} {sh.kind} inputs{extra}")
 
 
 class ClockSampler:
@@ -222,14 +225,17 @@ def main():
     sptr = stream.cuda_stream
     api.load_library()
 
+    p_mode = api.ZYFA_P_EXACT if args.p_mode == "exact" else api.ZYFA_P_LEAN
+
     def step(q, k, v, o):
-        st = api.zyfa_attn_fwd_causal(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), sh.B, sh.S, sh.H,
-                                      sh.H_kv, sh.D_qk, sh.D_v, 0.0, dtype_code,
-                                      desc.data_ptr() if args.dtype == "fp8" else 0,
-                                      desc.data_ptr() + 4 if args.dtype == "fp8" else 0,
-                                      desc.data_ptr() + 8 if args.dtype == "fp8" else 0, sptr)
+        st = api.zyfa_attn_fwd_causal_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), sh.B, sh.S, sh.H,
+                                         sh.H_kv, sh.D_qk, sh.D_v, 0.0, dtype_code,
+                                         desc.data_ptr() if args.dtype == "fp8" else 0,
+                                         desc.data_ptr() + 4 if args.dtype == "fp8" else 0,
+                                         desc.data_ptr() + 8 if args.dtype == "fp8" else 0, p_mode=p_mode,
+                                         stream=sptr)
         if st != 0:
-            raise api.ZyfaError(st, "zyfa_attn_fwd_causal")
+            raise api.ZyfaError(st, "zyfa_attn_fwd_causal_ex")
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -314,14 +320,14 @@ def main():
         if os.path.exists(tpath):
             with open(tpath) as f:
                 td = json.load(f)
-            key = f"{args.dtype}:{args.config}"
+            key = f"{args.dtype}:{args.config}" + (":exact" if args.p_mode == "exact" else "")
             if key in td and not args.heads and td[key].get("kernel_sha256") == kernel_source_hash():
                 traffic = td[key].get("bytes_per_launch")
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3" if is_fp8 else "bf16", "data": "synthetic",
-            "config": {"workload": workload_name(sh, args.dtype), "l2": "inputs 192 MB + output 256 MB per step "
+            "config": {"workload": workload_name(sh, args.dtype, args.p_mode), "l2": "inputs 192 MB + output 256 MB per step "
                        "exceed the 129 MB L2; no flush" if sh.S >= 16384 else "working set may fit in L2",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "value_dense_formula": 2.0 * value,

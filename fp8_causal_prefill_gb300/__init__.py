@@ -6,4 +6,4 @@ only marshals arguments to it.  Importing the package does not load the library:
 does, and it raises if the library is missing.
 """
 from .api import (ZyfaError, flash_attn_func, library_path, load_library,  # noqa: F401
-                  zyfa_attn_fwd_causal, zyfa_check_errors, zyfa_kernel_launches)
+                  zyfa_attn_fwd_causal, zyfa_attn_fwd_causal_ex, zyfa_check_errors, zyfa_kernel_launches)

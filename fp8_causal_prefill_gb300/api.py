@@ -21,8 +21,15 @@ ZYFA_DTYPE_E4M3 = 0
 ZYFA_DTYPE_BF16 = 1
 STATUS = {0: "ZYFA_OK", 1: "ZYFA_ERR_INVALID_ARG", 2: "ZYFA_ERR_UNSUPPORTED", 3: "ZYFA_ERR_MISALIGNED",
           4: "ZYFA_ERR_CUDA", 5: "ZYFA_ERR_TIMEOUT"}
-EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_check_errors", "zyfa_status_string", "zyfa_kernel_launches",
-            "zyfa_selftest_stalled_pipeline")
+EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_attn_fwd_causal_ex", "zyfa_check_errors", "zyfa_status_string",
+            "zyfa_kernel_launches", "zyfa_selftest_stalled_pipeline")
+ZYFA_P_LEAN = 0
+ZYFA_P_EXACT = 1
+
+
+class FwdOptions(ctypes.Structure):
+    """zyfa_fwd_options_t: p_mode, descale_per_kv_head, lse (device pointer or None)."""
+    _fields_ = [("p_mode", ctypes.c_int), ("descale_per_kv_head", ctypes.c_int), ("lse", ctypes.c_void_p)]
 
 
 class ZyfaError(RuntimeError):
@@ -47,6 +54,9 @@ def load_library() -> ctypes.CDLL:
         vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.zyfa_attn_fwd_causal.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, vp, vp, vp]
         lib.zyfa_attn_fwd_causal.restype = ci
+        lib.zyfa_attn_fwd_causal_ex.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, vp, vp,
+                                                ctypes.POINTER(FwdOptions), vp]
+        lib.zyfa_attn_fwd_causal_ex.restype = ci
         lib.zyfa_selftest_stalled_pipeline.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp]
         lib.zyfa_selftest_stalled_pipeline.restype = ci
         lib.zyfa_check_errors.argtypes = [vp]
@@ -68,6 +78,18 @@ def zyfa_attn_fwd_causal(q: int, k: int, v: int, out: int, B: int, S: int, H: in
                                     q_descale or None, k_descale or None, v_descale or None, stream or None)
 
 
+def zyfa_attn_fwd_causal_ex(q: int, k: int, v: int, out: int, B: int, S: int, H: int, H_kv: int, D_qk: int,
+                            D_v: int, softmax_scale: float, dtype: int, q_descale: int = 0, k_descale: int = 0,
+                            v_descale: int = 0, p_mode: int = ZYFA_P_LEAN, descale_per_kv_head: int = 0,
+                            lse: int = 0, stream: int = 0) -> int:
+    """Call the C entry point with options (raw addresses); returns the status code."""
+    lib = load_library()
+    opts = FwdOptions(p_mode, descale_per_kv_head, lse or None)
+    return lib.zyfa_attn_fwd_causal_ex(q, k, v, out, B, S, H, H_kv, D_qk, D_v, float(softmax_scale), dtype,
+                                       q_descale or None, k_descale or None, v_descale or None,
+                                       ctypes.byref(opts), stream or None)
+
+
 def zyfa_selftest_stalled_pipeline(q: int, k: int, v: int, out: int, B: int, S: int, H: int, H_kv: int, D_qk: int,
                                    D_v: int, dtype: int, stream: int = 0) -> int:
     """Enqueue the kernel with its loads withheld (tests of the timeout path); returns the status code."""
@@ -83,22 +105,31 @@ def zyfa_kernel_launches(B: int, S: int, H: int) -> int:
     return load_library().zyfa_kernel_launches(B, S, H)
 
 
-def _ptr_or_zero(t):
+def _descale_ptr(t, per_head_numel):
+    """(pointer, per_head) for a descale tensor: one float (per tensor) or per_head_numel floats
+    ([batch][KV head], flash_attn_func's (batch, nheads_k) layout)."""
     if t is None:
-        return 0
-    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32 and t.numel() == 1):
-        raise TypeError("descale must be a 1-element float32 CUDA tensor or None")
-    return t.data_ptr()
+        return 0, None
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+        raise TypeError("descale must be a contiguous float32 CUDA tensor or None")
+    if t.numel() == 1:
+        return t.data_ptr(), False
+    if t.numel() == per_head_numel:
+        return t.data_ptr(), True
+    raise ValueError(f"descale must hold 1 or batch*nheads_k = {per_head_numel} values, got {t.numel()}")
 
 
 def flash_attn_func(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: float | None = None,
                     causal: bool = True, q_descale=None, k_descale=None, v_descale=None,
-                    out: torch.Tensor | None = None) -> torch.Tensor:
+                    out: torch.Tensor | None = None, return_lse: bool = False, p_mode: str = "lean"):
     """Causal prefill attention on CUDA tensors q [B,S,H,D_qk], k [B,S,H_kv,D_qk], v [B,S,H_kv,D_v].
 
     FP8 inputs are ``torch.float8_e4m3fn`` (or ``torch.uint8`` holding e4m3 bit patterns) with optional
-    per-tensor descales (1-element float32 CUDA tensors); BF16 inputs are ``torch.bfloat16``.  Returns a
-    bfloat16 tensor [B,S,H,D_v].  Runs on the current CUDA stream.
+    descales: float32 CUDA tensors of one value (per tensor) or of B*H_kv values ([batch][KV head]); all
+    three given descales must use the same form.  BF16 inputs are ``torch.bfloat16``.  ``p_mode`` picks
+    how FP8 probabilities are produced ("lean": Lean P; "exact": exponential and e4m3 rounding).
+    Returns a bfloat16 tensor [B,S,H,D_v], and with ``return_lse`` also the float32 log-sum-exp
+    [B,H,S].  Runs on the current CUDA stream.
     """
     if not causal:
         raise NotImplementedError("only causal attention is implemented")
@@ -123,12 +154,20 @@ def flash_attn_func(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_s
         out = torch.empty((B, S, H, D_v), dtype=torch.bfloat16, device=q.device)
     elif out.shape != (B, S, H, D_v) or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous bfloat16 [B,S,H,D_v] tensor")
+    if p_mode not in ("lean", "exact"):
+        raise ValueError("p_mode must be 'lean' or 'exact'")
+    descales = [_descale_ptr(t, B * H_kv) for t in (q_descale, k_descale, v_descale)]
+    forms = {per for _, per in descales if per is not None}
+    if len(forms) > 1:
+        raise ValueError("descales must all be per tensor or all per (batch, KV head)")
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if return_lse else None
     stream = torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
-        st = zyfa_attn_fwd_causal(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, H, H_kv, D_qk,
-                                  D_v, 0.0 if softmax_scale is None else softmax_scale, dtype,
-                                  _ptr_or_zero(q_descale), _ptr_or_zero(k_descale), _ptr_or_zero(v_descale),
-                                  stream)
+        st = zyfa_attn_fwd_causal_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, H, H_kv, D_qk,
+                                     D_v, 0.0 if softmax_scale is None else softmax_scale, dtype,
+                                     descales[0][0], descales[1][0], descales[2][0],
+                                     ZYFA_P_EXACT if p_mode == "exact" else ZYFA_P_LEAN,
+                                     1 if forms == {True} else 0, lse.data_ptr() if lse is not None else 0, stream)
     if st != 0:
-        raise ZyfaError(st, "zyfa_attn_fwd_causal")
-    return out
+        raise ZyfaError(st, "zyfa_attn_fwd_causal_ex")
+    return (out, lse) if return_lse else out

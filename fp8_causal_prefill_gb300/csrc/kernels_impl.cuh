@@ -10,11 +10,11 @@ int smem_bytes() {
   return Cfg<FP8, DQK, DV, tile_keys<FP8, DQK, DV>()>::kSmemBytes;
 }
 
-template <bool FP8, int DQK, int DV>
+template <bool FP8, int DQK, int DV, bool EXACT>
 cudaError_t launch_fwd(const LaunchArgs& a) {
   constexpr int BN = tile_keys<FP8, DQK, DV>();
   using C = Cfg<FP8, DQK, DV, BN>;
-  auto kernel = zyfa_fwd_kernel<FP8, DQK, DV, BN>;
+  auto kernel = zyfa_fwd_kernel<FP8, DQK, DV, BN, EXACT>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
   Params p;
@@ -30,6 +30,8 @@ cudaError_t launch_fwd(const LaunchArgs& a) {
   p.num_units = a.num_units;
   p.status = a.status;
   p.stall_loads = a.stall_loads;
+  p.lse = a.lse;
+  p.desc_per_head = a.desc_per_head;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(kThreads);

@@ -19,7 +19,9 @@ struct LaunchArgs {
   float softmax_scale;
   int num_units;
   int* status;
-  int stall_loads;  // nonzero only for the stalled-pipeline self-test
+  int stall_loads;    // nonzero only for the stalled-pipeline self-test
+  float* lse;         // optional log-sum-exp output [B,H,S]
+  int desc_per_head;  // descales indexed by (batch, KV head)
   int grid;
   Maps maps;
   cudaStream_t stream;
@@ -31,9 +33,9 @@ constexpr int tile_keys() {
   return (!FP8 && DQK == 192) ? 64 : 128;
 }
 
-// Defined for <true,64,64>, <true,128,128>, <true,192,128> in zyfa_kernels_fp8.cu and for the same
-// head shapes with FP8 = false in zyfa_kernels_bf16.cu.
-template <bool FP8, int DQK, int DV>
+// Defined for the head shapes (64,64), (128,128), (192,128): FP8 with Lean P in zyfa_kernels_fp8.cu,
+// FP8 with exact P (EXACT = true) in zyfa_kernels_fp8_exact.cu, BF16 in zyfa_kernels_bf16.cu.
+template <bool FP8, int DQK, int DV, bool EXACT>
 cudaError_t launch_fwd(const LaunchArgs& a);
 
 // Dynamic shared memory the kernel instantiation needs (bytes).

@@ -70,7 +70,7 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, int D, int heads, int 
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8, int DQK, int DV>
+template <bool FP8, int DQK, int DV, bool EXACT>
 zyfa_status_t run(zyfa::LaunchArgs& a, const void* q, const void* k, const void* v) {
   constexpr int es = FP8 ? 1 : 2;
   constexpr int kRowK = DQK * es, kRowV = DV * es;
@@ -95,7 +95,7 @@ zyfa_status_t run(zyfa::LaunchArgs& a, const void* q, const void* k, const void*
   // maps the instantiation never touches are copies of valid ones
   if (kRowK < 128) { m.q0 = m.q1; m.k0 = m.k1; }
   if (kRowK % 128 != 64) { m.q1 = m.q0; m.k1 = m.k0; }
-  return zyfa::launch_fwd<FP8, DQK, DV>(a) == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
+  return zyfa::launch_fwd<FP8, DQK, DV, EXACT>(a) == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
 }  // namespace
@@ -124,9 +124,15 @@ namespace {
 // kernel's producer withhold every load (the self-test of the timeout path).
 zyfa_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int S, int H, int H_kv,
                        int D_qk, int D_v, float softmax_scale, zyfa_dtype_t dtype, const float* q_descale,
-                       const float* k_descale, const float* v_descale, cudaStream_t stream, int stall_loads) {
+                       const float* k_descale, const float* v_descale, const zyfa_fwd_options_t* opts,
+                       cudaStream_t stream, int stall_loads) {
   if (B < 1 || H < 1 || H_kv < 1 || S < 0 || H % H_kv != 0) return ZYFA_ERR_INVALID_ARG;
   if (dtype != ZYFA_DTYPE_E4M3 && dtype != ZYFA_DTYPE_BF16) return ZYFA_ERR_INVALID_ARG;
+  zyfa_fwd_options_t o = {ZYFA_P_LEAN, 0, nullptr};
+  if (opts) o = *opts;
+  if (o.p_mode != ZYFA_P_LEAN && o.p_mode != ZYFA_P_EXACT) return ZYFA_ERR_INVALID_ARG;
+  if (o.descale_per_kv_head != 0 && o.descale_per_kv_head != 1) return ZYFA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(o.lse) & 3u) != 0) return ZYFA_ERR_MISALIGNED;
   if (!std::isfinite(softmax_scale) || softmax_scale < 0.0f) return ZYFA_ERR_INVALID_ARG;
   const bool shape_ok = (D_qk == 64 && D_v == 64) || (D_qk == 128 && D_v == 128) || (D_qk == 192 && D_v == 128);
   if (!shape_ok) return ZYFA_ERR_UNSUPPORTED;
@@ -163,14 +169,21 @@ zyfa_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, i
   a.grid = static_cast<int>(units < nsm ? units : nsm);
   a.stream = stream;
   a.stall_loads = stall_loads;
-  if (fp8) {
-    if (D_qk == 64) return run<true, 64, 64>(a, q, k, v);
-    if (D_qk == 128) return run<true, 128, 128>(a, q, k, v);
-    return run<true, 192, 128>(a, q, k, v);
+  a.lse = o.lse;
+  a.desc_per_head = fp8 ? o.descale_per_kv_head : 0;
+  if (fp8 && o.p_mode == ZYFA_P_EXACT) {
+    if (D_qk == 64) return run<true, 64, 64, true>(a, q, k, v);
+    if (D_qk == 128) return run<true, 128, 128, true>(a, q, k, v);
+    return run<true, 192, 128, true>(a, q, k, v);
   }
-  if (D_qk == 64) return run<false, 64, 64>(a, q, k, v);
-  if (D_qk == 128) return run<false, 128, 128>(a, q, k, v);
-  return run<false, 192, 128>(a, q, k, v);
+  if (fp8) {
+    if (D_qk == 64) return run<true, 64, 64, false>(a, q, k, v);
+    if (D_qk == 128) return run<true, 128, 128, false>(a, q, k, v);
+    return run<true, 192, 128, false>(a, q, k, v);
+  }
+  if (D_qk == 64) return run<false, 64, 64, false>(a, q, k, v);
+  if (D_qk == 128) return run<false, 128, 128, false>(a, q, k, v);
+  return run<false, 192, 128, false>(a, q, k, v);
 }
 
 }  // namespace
@@ -182,13 +195,22 @@ zyfa_status_t zyfa_attn_fwd_causal(const void* q, const void* k, const void* v, 
                                    const float* q_descale, const float* k_descale, const float* v_descale,
                                    cudaStream_t stream) {
   return attn_fwd(q, k, v, out, B, S, H, H_kv, D_qk, D_v, softmax_scale, dtype, q_descale, k_descale, v_descale,
-                  stream, 0);
+                  nullptr, stream, 0);
+}
+
+zyfa_status_t zyfa_attn_fwd_causal_ex(const void* q, const void* k, const void* v, void* out, int B, int S, int H,
+                                      int H_kv, int D_qk, int D_v, float softmax_scale, zyfa_dtype_t dtype,
+                                      const float* q_descale, const float* k_descale, const float* v_descale,
+                                      const zyfa_fwd_options_t* options, cudaStream_t stream) {
+  return attn_fwd(q, k, v, out, B, S, H, H_kv, D_qk, D_v, softmax_scale, dtype, q_descale, k_descale, v_descale,
+                  options, stream, 0);
 }
 
 zyfa_status_t zyfa_selftest_stalled_pipeline(const void* q, const void* k, const void* v, void* out, int B, int S,
                                              int H, int H_kv, int D_qk, int D_v, zyfa_dtype_t dtype,
                                              cudaStream_t stream) {
-  return attn_fwd(q, k, v, out, B, S, H, H_kv, D_qk, D_v, 0.0f, dtype, nullptr, nullptr, nullptr, stream, 1);
+  return attn_fwd(q, k, v, out, B, S, H, H_kv, D_qk, D_v, 0.0f, dtype, nullptr, nullptr, nullptr, nullptr, stream,
+                  1);
 }
 
 zyfa_status_t zyfa_check_errors(cudaStream_t stream) {

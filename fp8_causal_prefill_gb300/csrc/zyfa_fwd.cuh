@@ -131,6 +131,8 @@ struct Params {
   int num_units;  // B*H*ceil(S/256)
   int* status;    // device status word (timeouts)
   int stall_loads;  // self-test of the timeout path: the producer withholds every load
+  float* lse;       // optional [B,H,S] natural-log sum of exp of the scores (nullptr: not written)
+  int desc_per_head;  // descales are arrays [B][H_kv] (1) or single values (0)
 };
 
 struct __align__(8) SharedCtl {
@@ -256,7 +258,29 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, float f) {
   }
 }
 
-template <bool FP8, int DQK, int DV, int BN>
+// Two fp32 -> e4m3 codes (round to nearest even, saturating), the upper byte takes `hi`.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Exact-P codes of the 64 scores of one scale block with exponent e: the probability
+// 2^(s*a/8 - e) from the hardware exponential, rounded to e4m3.  The comparison point for Lean P
+// (one exponential per probability, exactly rounded).
+__device__ __forceinline__ void exactp_block(const float* s, float a8, int e, uint32_t (&pw)[16]) {
+  const float ne = -static_cast<float>(e);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float p0 = ex2(__fmaf_rn(s[4 * i + 0], a8, ne));
+    const float p1 = ex2(__fmaf_rn(s[4 * i + 1], a8, ne));
+    const float p2 = ex2(__fmaf_rn(s[4 * i + 2], a8, ne));
+    const float p3 = ex2(__fmaf_rn(s[4 * i + 3], a8, ne));
+    pw[i] = cvt_e4m3x2(p1, p0) | (cvt_e4m3x2(p3, p2) << 16);
+  }
+}
+
+template <bool FP8, int DQK, int DV, int BN, bool EXACT>
 __global__ void __launch_bounds__(kThreads, 1)
     zyfa_fwd_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
   using C = Cfg<FP8, DQK, DV, BN>;
@@ -579,16 +603,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_addr + C::col_o(t);
     const uint32_t tP = tmem + lane_addr + C::col_p(t);
 
-    float a;
-    if constexpr (FP8) {
-      const float dq = p.q_descale ? *p.q_descale : 1.0f;
-      const float dk = p.k_descale ? *p.k_descale : 1.0f;
-      a = __fmul_rn(__fmul_rn(__fmul_rn(p.softmax_scale, dq), dk), 11.541560327111707f);
-    } else {
-      a = __fmul_rn(p.softmax_scale, 1.4426950408889634f);
-    }
-    const float out_scale = (FP8 && p.v_descale) ? *p.v_descale : 1.0f;
-    const float a24 = a * 0x1p-24f;  // exact: scales Lean-P values into f16 subnormal units
+    // score scale a (FP8: 1/8-binade units, with the descales; BF16: binades) and output scale dv,
+    // per unit when the descales are per (batch, KV head)
+    auto unit_scales = [&](const Unit& un, float& a_, float& out_) {
+      if constexpr (FP8) {
+        const int di = p.desc_per_head ? un.b * p.H_kv + un.h / (p.H / p.H_kv) : 0;
+        const float dq = p.q_descale ? p.q_descale[di] : 1.0f;
+        const float dk = p.k_descale ? p.k_descale[di] : 1.0f;
+        a_ = __fmul_rn(__fmul_rn(__fmul_rn(p.softmax_scale, dq), dk), 11.541560327111707f);
+        out_ = p.v_descale ? p.v_descale[di] : 1.0f;
+      } else {
+        a_ = __fmul_rn(p.softmax_scale, 1.4426950408889634f);
+        out_ = 1.0f;
+      }
+    };
     if constexpr (FP8) {
       if (t == 0) {
         // e8m0 scale factors of V (all 1.0), written once; every PV is issued after an arrival of
@@ -610,6 +638,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row0 = u.r0 + t * kBlockM;  // first row of the tile
       const int row = row0 + rloc;
       const bool row_ok = row < p.S;
+      float a, out_scale;
+      unit_scales(u, a, out_scale);
+      const float a24 = a * 0x1p-24f;  // exact: scales Lean-P values into f16 subnormal units
+      const float a8 = a * 0.125f;     // exact: binade units for the exact-P exponential
 
       int m_ref = 0;
       float l_bf16 = 0.0f;  // BF16: fp32 sum of the rounded probabilities of this row
@@ -666,7 +698,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int b = 0; b < kNB; ++b) {
             const int eb = e[b] == kNoExp ? m_ref : e[b];
-            leanp_block(s + 64 * b, a24, eb, *reinterpret_cast<uint32_t(*)[16]>(pw + 16 * b));
+            if constexpr (EXACT) exactp_block(s + 64 * b, a8, eb, *reinterpret_cast<uint32_t(*)[16]>(pw + 16 * b));
+            else leanp_block(s + 64 * b, a24, eb, *reinterpret_cast<uint32_t(*)[16]>(pw + 16 * b));
             int sf = 127 + eb - m_ref;
             sf = sf < 0 ? 0 : (sf > 254 ? 254 : sf);
             sfw |= static_cast<uint32_t>(sf) * (0x0101u << (16 * b));
@@ -718,6 +751,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = l_bf16;
       }
       const float inv = __fdiv_rn(out_scale, l);
+      if (p.lse != nullptr && row_ok) {
+        // ln sum_j exp(s_ij) = (M + log2 l) ln 2: l sums the rounded weights relative to 2^M
+        p.lse[(static_cast<size_t>(u.b) * p.H + u.h) * p.S + row] =
+            (static_cast<float>(m_ref) + __log2f(l)) * 0.6931471805599453f;
+      }
       __nv_bfloat16* orow = p.out + ((static_cast<size_t>(u.b) * p.S + (row_ok ? row : 0)) * p.H + u.h) * DV;
 #pragma unroll
       for (int c = 0; c < DV / 32; ++c) {

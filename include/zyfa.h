@@ -74,6 +74,37 @@ zyfa_status_t zyfa_attn_fwd_causal(const void* q, const void* k, const void* v, 
                                    zyfa_dtype_t dtype, const float* q_descale, const float* k_descale,
                                    const float* v_descale, cudaStream_t stream);
 
+/* How FP8 probabilities are produced (ZYFA abstract, technique (1); captivela ZYFA article, "Tiga Trik"). */
+typedef enum {
+  ZYFA_P_LEAN = 0, /* Lean P: one multiply-add and one rounding per probability (the default)       */
+  ZYFA_P_EXACT = 1 /* exact P: hardware exponential, then e4m3 rounding (the pages' comparison point)  */
+} zyfa_p_mode_t;
+
+/* Optional behaviour of zyfa_attn_fwd_causal_ex.  A zero-initialised struct (or NULL) gives the
+ * behaviour of zyfa_attn_fwd_causal. */
+typedef struct {
+  zyfa_p_mode_t p_mode;    /* FP8 only; BF16 always exponentiates exactly (ignored there)          */
+  int descale_per_kv_head; /* FP8 only: 0 = each descale points to one float; 1 = to B*H_kv floats,
+                              [b][hk], the descale of batch b and KV head hk (flash_attn_func's
+                              (batch, nheads_k) descale tensors); query head h uses hk = h/(H/H_kv) */
+  float* lse;              /* NULL, or a device pointer to B*H*S floats, [b][h][i], 4-byte aligned:
+                              receives ln sum_{j<=i} exp(scale * q_i . k_j) in real (descaled) units,
+                              from the same rounded weights that normalise the output */
+} zyfa_fwd_options_t;
+
+/*
+ * zyfa_attn_fwd_causal_ex - zyfa_attn_fwd_causal with the options above (flash_attn_func's
+ * softmax_lse output and per-(batch, KV head) descales; exact P for the Lean-P ablation).
+ * `options` may be NULL.  Same layouts, ownership, asynchrony and errors as zyfa_attn_fwd_causal;
+ * additionally ZYFA_ERR_INVALID_ARG for an unknown p_mode or a descale_per_kv_head other than 0/1,
+ * ZYFA_ERR_MISALIGNED for an lse pointer that is not 4-byte aligned.
+ */
+zyfa_status_t zyfa_attn_fwd_causal_ex(const void* q, const void* k, const void* v, void* out, int B, int S,
+                                      int H, int H_kv, int D_qk, int D_v, float softmax_scale,
+                                      zyfa_dtype_t dtype, const float* q_descale, const float* k_descale,
+                                      const float* v_descale, const zyfa_fwd_options_t* options,
+                                      cudaStream_t stream);
+
 /*
  * zyfa_check_errors - synchronise `stream`, then read and clear the current device's status word.
  * Returns ZYFA_ERR_TIMEOUT if any kernel of this library timed out since the last check,

@@ -69,3 +69,23 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(api, "_lib", None)
     with pytest.raises(api.ZyfaError):
         api.load_library()
+
+
+def test_options_validation(lib):
+    import ctypes as ct
+    bad_mode = api.FwdOptions(7, 0, None)
+    st = lib.zyfa_attn_fwd_causal_ex(16, 16, 16, 16, 1, 8, 2, 2, 128, 128, 0.0, 0, None, None, None,
+                                     ct.byref(bad_mode), None)
+    assert st == 1
+    bad_flag = api.FwdOptions(0, 2, None)
+    st = lib.zyfa_attn_fwd_causal_ex(16, 16, 16, 16, 1, 8, 2, 2, 128, 128, 0.0, 0, None, None, None,
+                                     ct.byref(bad_flag), None)
+    assert st == 1
+    odd_lse = api.FwdOptions(0, 0, 18)
+    st = lib.zyfa_attn_fwd_causal_ex(16, 16, 16, 16, 1, 8, 2, 2, 128, 128, 0.0, 0, None, None, None,
+                                     ct.byref(odd_lse), None)
+    assert st == 3
+    # S == 0 with valid options returns OK without touching the device
+    ok = api.FwdOptions(1, 1, None)
+    assert lib.zyfa_attn_fwd_causal_ex(16, 16, 16, 16, 1, 0, 2, 2, 128, 128, 0.0, 0, None, None, None,
+                                       ct.byref(ok), None) == 0
