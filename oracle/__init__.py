@@ -17,6 +17,8 @@ Functions and the passages they follow (page title, section):
 * ``return_lse=True`` on O1, O2, O2x, O4: ln sum_j exp(s_ij) per row (flash_attn_func's softmax_lse).
 * ``plain_fp8_causal_attention`` (O3): exact-exponential FP8 softmax, comparison only.
 * ``bf16_causal_attention`` (O4): the BF16 twin (the pages give no BF16 numerics; plainest reading).
+* ``hadamard``: Hadamard rotation of Q and K before quantisation (spbcomputers.ru ZYFA article, FAQ
+  "Что даёт поворот Адамара?"; captivela ZYFA article, "Angka Nyata").
 """
 from .formats import (E4M3_MAX, bf16_bits_to_float, bf16_round, e4m3_decode,  # noqa: F401
                       e4m3_encode_rne_satfinite, fl32)
@@ -25,3 +27,5 @@ from .attention import (LEANP_C0, SCALE_BLOCK, bf16_causal_attention,  # noqa: F
                         exact_causal_attention, exactp_causal_attention, exactp_code, fp8_score_scale,
                         leanp_causal_attention, leanp_code,
                         leanp_row_weights, plain_fp8_causal_attention, rel_l2)
+from .hadamard import (fwht_f32, hadamard_block, hadamard_matrix, hadamard_quantize_e4m3,  # noqa: F401
+                       rotate)
