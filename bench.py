@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--dtype", choices=["fp8", "bf16"], default="fp8")
     ap.add_argument("--config", default="bench32k")
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling a smaller case)")
+    ap.add_argument("--hadamard", action="store_true",
+                    help="also time the Hadamard rotation + quantisation pre-pass of Q and K (bf16 in)")
     ap.add_argument("--p-mode", choices=["lean", "exact"], default="lean",
                     help="FP8 probabilities: Lean P (the method) or exact exponential (the ablation)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -274,6 +276,43 @@ def main():
     if zst != 0:
         raise api.ZyfaError(zst, "kernel status")
 
+    # the Hadamard pre-pass of Q and K (bf16 -> rotated e4m3 + descale), timed on its own
+    prepass = None
+    if args.hadamard:
+        from fp8_causal_prefill_gb300.inputs import make_problem as _mk
+        pb = p if p.qb is not None else _mk(sh, seed=rank, bf16=True, fp8=False)
+        xq, xk = pb.qb.to(dev), pb.kb.to(dev)
+        outs = [(torch.empty(x.shape, dtype=torch.uint8, device=dev), torch.empty(1, dtype=torch.float32, device=dev),
+                 torch.empty(max(1, api.zyfa_hadamard_workspace_bytes(x.numel() // sh.D_qk) // 4),
+                             dtype=torch.float32, device=dev)) for x in (xq, xk)]
+
+        def prestep():
+            for x, (c, d, ws) in zip((xq, xk), outs):
+                st = api.zyfa_hadamard_quantize_e4m3(x.data_ptr(), c.data_ptr(), d.data_ptr(), x.numel() // sh.D_qk,
+                                                     sh.D_qk, ws.data_ptr(), ws.numel() * 4, sptr)
+                if st != 0:
+                    raise api.ZyfaError(st, "zyfa_hadamard_quantize_e4m3")
+        for _ in range(3):
+            prestep()
+        barrier()
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_pre = 20
+        h0.record(stream)
+        for _ in range(n_pre):
+            prestep()
+        h1.record(stream)
+        barrier()
+        pre_ms = h0.elapsed_time(h1) / n_pre
+        elems = xq.numel() + xk.numel()
+        alg_bytes = 3 * elems      # bf16 read once + e4m3 written once
+        moved = 5 * elems          # two passes read the bf16 input
+        hbm = load_peaks()[0].get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        prepass = {"ms": pre_ms, "fraction_of_attention": pre_ms / ms_per_step,
+                   "algorithmic_bytes": alg_bytes, "bytes_moved": moved,
+                   "achieved_gbs": moved / (pre_ms * 1e-3) / 1e9,
+                   "hbm_frac": moved / (pre_ms * 1e-3) / 1e9 / hbm,
+                   "launches_per_step": 4, "what": "Q and K of the workload, bf16 -> rotated e4m3 + descale"}
+
     # end to end through the same C entry point with host buffers: H2D of q/k/v, the call, D2H of out
     e2e = None
     if not args.no_e2e:
@@ -343,6 +382,8 @@ def main():
         }
         if e2e is not None:
             line["e2e"] = e2e
+        if prepass is not None:
+            line["hadamard_prepass"] = prepass
         if not args.no_cpu and world == 1:
             line["cpu_baseline"] = cpu_oracle_sample(p, args.dtype, args.cpu_seconds)
         print(json.dumps(line), flush=True)

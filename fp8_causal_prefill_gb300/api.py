@@ -22,7 +22,8 @@ ZYFA_DTYPE_BF16 = 1
 STATUS = {0: "ZYFA_OK", 1: "ZYFA_ERR_INVALID_ARG", 2: "ZYFA_ERR_UNSUPPORTED", 3: "ZYFA_ERR_MISALIGNED",
           4: "ZYFA_ERR_CUDA", 5: "ZYFA_ERR_TIMEOUT"}
 EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_attn_fwd_causal_ex", "zyfa_check_errors", "zyfa_status_string",
-            "zyfa_kernel_launches", "zyfa_selftest_stalled_pipeline")
+            "zyfa_kernel_launches", "zyfa_selftest_stalled_pipeline", "zyfa_hadamard_quantize_e4m3",
+            "zyfa_hadamard_workspace_bytes")
 ZYFA_P_LEAN = 0
 ZYFA_P_EXACT = 1
 
@@ -59,6 +60,11 @@ def load_library() -> ctypes.CDLL:
         lib.zyfa_attn_fwd_causal_ex.restype = ci
         lib.zyfa_selftest_stalled_pipeline.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp]
         lib.zyfa_selftest_stalled_pipeline.restype = ci
+        ll, sz = ctypes.c_longlong, ctypes.c_size_t
+        lib.zyfa_hadamard_quantize_e4m3.argtypes = [vp, vp, vp, ll, ci, vp, sz, vp]
+        lib.zyfa_hadamard_quantize_e4m3.restype = ci
+        lib.zyfa_hadamard_workspace_bytes.argtypes = [ll]
+        lib.zyfa_hadamard_workspace_bytes.restype = sz
         lib.zyfa_check_errors.argtypes = [vp]
         lib.zyfa_check_errors.restype = ci
         lib.zyfa_status_string.argtypes = [ci]
@@ -171,3 +177,34 @@ def flash_attn_func(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_s
     if st != 0:
         raise ZyfaError(st, "zyfa_attn_fwd_causal_ex")
     return (out, lse) if return_lse else out
+
+
+def zyfa_hadamard_quantize_e4m3(x: int, x8: int, descale: int, rows: int, D: int, workspace: int,
+                                workspace_bytes: int, stream: int = 0) -> int:
+    """Call the C pre-pass with raw addresses; returns the status code."""
+    return load_library().zyfa_hadamard_quantize_e4m3(x or None, x8 or None, descale or None, rows, D,
+                                                      workspace or None, workspace_bytes, stream or None)
+
+
+def zyfa_hadamard_workspace_bytes(rows: int) -> int:
+    return load_library().zyfa_hadamard_workspace_bytes(rows)
+
+
+def hadamard_quantize_e4m3(x: torch.Tensor):
+    """Rotate a bf16 CUDA tensor [..., D] by the block Hadamard matrix over its last axis and quantise
+    it per tensor to e4m3.  Returns (codes as torch.float8_e4m3fn, same shape; descale, a 1-element
+    float32 CUDA tensor).  Rotate Q and K (not V) and pass the codes and descales to flash_attn_func."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous bfloat16 CUDA tensor")
+    D = x.shape[-1]
+    rows = x.numel() // D if D else 0
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    descale = torch.ones(1, dtype=torch.float32, device=x.device)
+    ws = torch.empty(max(1, zyfa_hadamard_workspace_bytes(rows) // 4), dtype=torch.float32, device=x.device)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    with torch.cuda.device(x.device):
+        st = zyfa_hadamard_quantize_e4m3(x.data_ptr(), codes.data_ptr(), descale.data_ptr(), rows, D,
+                                         ws.data_ptr(), ws.numel() * 4, stream)
+    if st != 0:
+        raise ZyfaError(st, "zyfa_hadamard_quantize_e4m3")
+    return codes.view(torch.float8_e4m3fn), descale

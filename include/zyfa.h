@@ -27,6 +27,7 @@
 #define ZYFA_H_
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -104,6 +105,34 @@ zyfa_status_t zyfa_attn_fwd_causal_ex(const void* q, const void* k, const void* 
                                       zyfa_dtype_t dtype, const float* q_descale, const float* k_descale,
                                       const float* v_descale, const zyfa_fwd_options_t* options,
                                       cudaStream_t stream);
+
+/*
+ * zyfa_hadamard_quantize_e4m3 - Hadamard rotation and per-tensor FP8 quantisation of Q or K, the
+ * pre-pass that roughly halves the error input quantisation adds to attention (spbcomputers.ru ZYFA
+ * article, FAQ "Что даёт поворот Адамара?"; captivela ZYFA article, "Angka Nyata").  Rotating Q and K
+ * by the same orthogonal matrix leaves attention unchanged, so the codes go straight into
+ * zyfa_attn_fwd_causal (V is not rotated).
+ *
+ *   x          device pointer, bf16 [rows][D] (e.g. q [B,S,H,D] with rows = B*S*H), 16-byte aligned.
+ *   x8         device pointer, e4m3 codes [rows][D], 16-byte aligned; written in full.
+ *   descale    device pointer to one float, 4-byte aligned: receives the per-tensor descale
+ *              fl32(max|y| / 448) (1.0 if every rotated value is 0), ready to pass as q/k_descale.
+ *   rows, D    rows >= 0 (0: nothing is done), D in {64, 128, 192}.
+ *   workspace  device scratch of at least zyfa_hadamard_workspace_bytes(rows) bytes, 4-byte
+ *              aligned, owned by the caller; its contents on entry do not matter.
+ *
+ * y = x R with R block-diagonal over the head dimension: normalised Walsh-Hadamard blocks of 128
+ * (D = 128) or 64 (D = 64, 192), computed in fp32 by the radix-2 transform; codes =
+ * rne_e4m3_satfinite(fl32(y * fl32(448 / max|y|))).  Two kernel launches on `stream`, asynchronous; allocates
+ * nothing.  Errors: ZYFA_ERR_INVALID_ARG (null pointers, negative rows, short workspace),
+ * ZYFA_ERR_UNSUPPORTED (D, or rows*D beyond 2^40), ZYFA_ERR_MISALIGNED, ZYFA_ERR_CUDA (launch).
+ */
+zyfa_status_t zyfa_hadamard_quantize_e4m3(const void* x, void* x8, float* descale, long long rows, int D,
+                                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* zyfa_hadamard_workspace_bytes - workspace zyfa_hadamard_quantize_e4m3 needs for `rows` rows:
+ * one float per 128 rows (0 for rows <= 0).  Pure host arithmetic. */
+size_t zyfa_hadamard_workspace_bytes(long long rows);
 
 /*
  * zyfa_check_errors - synchronise `stream`, then read and clear the current device's status word.

@@ -13,9 +13,12 @@ Readings (the pages give no details):
 * R is block-diagonal over the head dimension with normalised Walsh-Hadamard blocks H_n / sqrt(n)
   (Sylvester order), n = 128 for D = 128 and n = 64 for D = 64 and D = 192 (three blocks).
 * The rotated values are computed in float32 by the radix-2 fast transform, stage h = 1, 2, 4, ...
-  (butterflies a+b, a-b), then multiplied by fl32(1/sqrt(n)); the quantiser then works on those
-  float32 values exactly as for unrotated inputs: descale = fl32(amax / 448) (1 if amax is 0) and
-  codes = rne_e4m3_satfinite(fl32(y / descale)).
+  (butterflies a+b, a-b), then multiplied by fl32(1/sqrt(n)).
+* They are quantised per tensor with the usual FP8 scale pair: scale = fl32(448 / amax) multiplies
+  every value, codes = rne_e4m3_satfinite(fl32(y * scale)), and descale = fl32(amax / 448) is what
+  dequantises (both 1 if amax is 0).  A multiply per element instead of a division; the codes agree
+  with the division recipe except where y*scale and y/descale round to different sides of a code
+  boundary (relative distance ~1e-7).
 """
 from __future__ import annotations
 
@@ -80,5 +83,6 @@ def hadamard_quantize_e4m3(x):
     y = fwht_f32(x, hadamard_block(x.shape[-1]))
     amax = np.float32(np.max(np.abs(y))) if y.size else np.float32(0.0)
     descale = np.float32(amax / E4M3_MAX_F32) if amax > 0 else np.float32(1.0)
-    codes = e4m3_encode_rne_satfinite((y / descale).astype(np.float32).astype(np.float64))
+    scale = np.float32(E4M3_MAX_F32 / amax) if amax > 0 else np.float32(1.0)
+    codes = e4m3_encode_rne_satfinite((y * scale).astype(np.float32).astype(np.float64))
     return codes, float(descale)

@@ -20,7 +20,7 @@ def lib():
 def _declared_functions():
     text = open(os.path.join(ROOT, "include", "zyfa.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(zyfa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(zyfa_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_abi():

@@ -69,7 +69,12 @@ def test_quantiser_matches_the_plain_recipe_on_rotated_values():
     x = rng.standard_normal((64, 128)).astype(np.float32)
     codes, ds = O.hadamard_quantize_e4m3(x)
     y = O.fwht_f32(x, 128)
-    assert ds == float(np.float32(np.float32(np.abs(y).max()) / np.float32(448.0)))
+    amax = np.float32(np.abs(y).max())
+    assert ds == float(np.float32(amax / np.float32(448.0)))
+    # the scale multiply agrees with the division recipe on all but a handful of boundary values
+    div = O.e4m3_encode_rne_satfinite((y / np.float32(ds)).astype(np.float32).astype(np.float64))
+    assert np.mean(div != codes) < 1e-3 and np.all(np.abs(div.astype(int) - codes.astype(int)) <= 1)
+    assert (codes & 0x7F).max() == 0x7E                         # the maximum maps to 448
     deq = O.e4m3_decode(codes) * ds
     assert np.abs(deq).max() <= 448.0 * ds * (1 + 1e-7)
     np.testing.assert_allclose(deq, y, rtol=1.0 / 16 + 1e-6, atol=2.0 ** -9 * ds)
