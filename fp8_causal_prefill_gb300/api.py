@@ -23,7 +23,7 @@ STATUS = {0: "ZYFA_OK", 1: "ZYFA_ERR_INVALID_ARG", 2: "ZYFA_ERR_UNSUPPORTED", 3:
           4: "ZYFA_ERR_CUDA", 5: "ZYFA_ERR_TIMEOUT"}
 EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_attn_fwd_causal_ex", "zyfa_check_errors", "zyfa_status_string",
             "zyfa_kernel_launches", "zyfa_selftest_stalled_pipeline", "zyfa_hadamard_quantize_e4m3",
-            "zyfa_hadamard_workspace_bytes")
+            "zyfa_hadamard_quantize_e4m3_noalloc", "zyfa_hadamard_workspace_bytes")
 ZYFA_P_LEAN = 0
 ZYFA_P_EXACT = 1
 
@@ -63,6 +63,8 @@ def load_library() -> ctypes.CDLL:
         ll, sz = ctypes.c_longlong, ctypes.c_size_t
         lib.zyfa_hadamard_quantize_e4m3.argtypes = [vp, vp, vp, ll, ci, vp, sz, vp]
         lib.zyfa_hadamard_quantize_e4m3.restype = ci
+        lib.zyfa_hadamard_quantize_e4m3_noalloc.argtypes = [vp, vp, vp, ll, ci, vp]
+        lib.zyfa_hadamard_quantize_e4m3_noalloc.restype = ci
         lib.zyfa_hadamard_workspace_bytes.argtypes = [ll]
         lib.zyfa_hadamard_workspace_bytes.restype = sz
         lib.zyfa_check_errors.argtypes = [vp]
@@ -184,6 +186,13 @@ def zyfa_hadamard_quantize_e4m3(x: int, x8: int, descale: int, rows: int, D: int
     """Call the C pre-pass with raw addresses; returns the status code."""
     return load_library().zyfa_hadamard_quantize_e4m3(x or None, x8 or None, descale or None, rows, D,
                                                       workspace or None, workspace_bytes, stream or None)
+
+
+def zyfa_hadamard_quantize_e4m3_noalloc(x: int, x8: int, descale: int, rows: int, D: int, stream: int = 0) -> int:
+    """Call the allocation-free C pre-pass (scratch inside the library; calls must not overlap on the
+    GPU); returns the status code."""
+    return load_library().zyfa_hadamard_quantize_e4m3_noalloc(x or None, x8 or None, descale or None, rows, D,
+                                                             stream or None)
 
 
 def zyfa_hadamard_workspace_bytes(rows: int) -> int:

@@ -147,6 +147,27 @@ __global__ void __launch_bounds__(kThreads) hadamard_quant_kernel(const __nv_bfl
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_nsm[kMaxDevices];
 
+// Scratch of the allocation-free entry point: the partial maxima (one float per 128 rows) live in
+// this fixed array, which every GPU that loads the library holds until the process exits.  128 KiB
+// covers 32768 partials, i.e. at most 4,194,304 rows per call.
+constexpr long long kNoAllocMaxPartials = 32768;
+constexpr long long kNoAllocMaxRows = kNoAllocMaxPartials * kRowsPerPartial;
+static __device__ __align__(256) float g_noalloc_partials[kNoAllocMaxPartials];
+// Device address of g_noalloc_partials per device, looked up once (in host code the array's name
+// is only a host-side stand-in, not a device address).
+std::atomic<float*> g_noalloc_ptr[kMaxDevices];
+
+float* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  float* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_noalloc_partials) != cudaSuccess || !addr) return nullptr;
+  g_noalloc_ptr[dev].store(static_cast<float*>(addr), std::memory_order_release);
+  return static_cast<float*>(addr);
+}
+
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
@@ -210,6 +231,19 @@ zyfa_status_t zyfa_hadamard_quantize_e4m3(const void* x, void* x8, float* descal
   if (!workspace || workspace_bytes < zyfa_hadamard_workspace_bytes(rows)) return ZYFA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 3u) return ZYFA_ERR_MISALIGNED;
   return dispatch(x, x8, descale, rows, D, static_cast<float*>(workspace), stream);
+}
+
+// The allocation-free variant: the same two kernels, with the partial maxima in the library's own
+// fixed device array instead of caller workspace.  Every slot the second kernel reads is written by
+// the first kernel of the same call, so nothing needs clearing between calls.
+zyfa_status_t zyfa_hadamard_quantize_e4m3_noalloc(const void* x, void* x8, float* descale, long long rows, int D,
+                                                  cudaStream_t stream) {
+  const zyfa_status_t st = check_args(x, x8, descale, rows, D);
+  if (st != ZYFA_OK || rows == 0) return st;
+  if (rows > kNoAllocMaxRows) return ZYFA_ERR_UNSUPPORTED;
+  float* scratch = noalloc_scratch();
+  if (!scratch) return ZYFA_ERR_CUDA;
+  return dispatch(x, x8, descale, rows, D, scratch, stream);
 }
 
 }  // extern "C"

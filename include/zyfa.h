@@ -130,6 +130,26 @@ zyfa_status_t zyfa_attn_fwd_causal_ex(const void* q, const void* k, const void* 
 zyfa_status_t zyfa_hadamard_quantize_e4m3(const void* x, void* x8, float* descale, long long rows, int D,
                                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * zyfa_hadamard_quantize_e4m3_noalloc - zyfa_hadamard_quantize_e4m3 without a workspace argument, for
+ * callers that cannot allocate device memory on their call path: a serving runtime whose device
+ * memory is planned up front and may not grow, or a plain C host program with no device allocator
+ * from which to hand over scratch.  The pages describe no such call; it is a convenience of this
+ * library.
+ *
+ * Same arguments, results and errors as zyfa_hadamard_quantize_e4m3, minus the workspace.  The
+ * scratch (the partial maxima) is a fixed 128 KiB array inside the library that every GPU which loads
+ * it holds until the process exits; it covers at most 4,194,304 rows per call, and larger calls return
+ * ZYFA_ERR_UNSUPPORTED without doing anything.  The call allocates nothing.  Its first call on a
+ * device looks up the array's device address (once per device, with that device current), so make
+ * that first call before any stream capture.  All calls share the one array: calls that overlap on
+ * the GPU (on different streams, or from several host threads, on the same device) race on it and
+ * may produce wrong codes; serialise them.  Nothing in the array needs to start at zero: each call
+ * writes every slot it later reads.
+ */
+zyfa_status_t zyfa_hadamard_quantize_e4m3_noalloc(const void* x, void* x8, float* descale, long long rows, int D,
+                                                  cudaStream_t stream);
+
 /* zyfa_hadamard_workspace_bytes - workspace zyfa_hadamard_quantize_e4m3 needs for `rows` rows:
  * one float per 128 rows (0 for rows <= 0).  Pure host arithmetic. */
 size_t zyfa_hadamard_workspace_bytes(long long rows);
