@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--dtype", choices=["fp8", "bf16"], default="fp8")
     ap.add_argument("--config", default="bench32k")
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling a smaller case)")
+    ap.add_argument("--energy", action="store_true",
+                    help="also measure energy per step (NVML total-energy counter over a >= 2 s loop)")
     ap.add_argument("--hadamard", action="store_true",
                     help="also time the Hadamard rotation + quantisation pre-pass of Q and K (bf16 in)")
     ap.add_argument("--p-mode", choices=["lean", "exact"], default="lean",
@@ -83,6 +85,39 @@ def workload_name(sh, dtype, p_mode="lean"):
     extra = ", exact-P ablation" if (dtype == "fp8" and p_mode == "exact") else ""
     return (f"{'e4m3' if dtype == 'fp8' else 'bf16'} causal prefill B={sh.B} H={sh.H} H_kv={sh.H_kv} S={sh.S} "
             f"D_qk={sh.D_qk} D_v={sh.D_v} {sh.kind} inputs{extra}")
+
+
+class EnergyCounter:
+    """Cumulative board energy of one GPU from NVML (read only), millijoules."""
+
+    def __init__(self, dev_index):
+        import ctypes
+        self.c = ctypes
+        self.nvml = None
+        self.h = ctypes.c_void_p()
+        try:
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                return
+            import torch
+            uuid = getattr(torch.cuda.get_device_properties(dev_index), "uuid", None)
+            ok = False
+            if uuid is not None:
+                ok = nvml.nvmlDeviceGetHandleByUUID(("GPU-" + str(uuid)).encode(), ctypes.byref(self.h)) == 0
+            if not ok:
+                ok = nvml.nvmlDeviceGetHandleByIndex_v2(dev_index, ctypes.byref(self.h)) == 0
+            if ok:
+                self.nvml = nvml
+        except OSError:
+            self.nvml = None
+
+    def read_mj(self):
+        if self.nvml is None:
+            return None
+        e = self.c.c_ulonglong(0)
+        if self.nvml.nvmlDeviceGetTotalEnergyConsumption(self.h, self.c.byref(e)) != 0:
+            return None
+        return int(e.value)
 
 
 class ClockSampler:
@@ -276,6 +311,28 @@ def main():
     if zst != 0:
         raise api.ZyfaError(zst, "kernel status")
 
+    # energy per step: NVML's cumulative energy counter around a loop of at least two seconds
+    energy = None
+    if args.energy and rank == 0:
+        meter = EnergyCounter(local)
+        n_en = max(args.steps, int(2.0 / max(ms_per_step * 1e-3, 1e-6)) + 1)
+        e_start = meter.read_mj()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(n_en):
+            step(dq, dk, dv, out)
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_end = meter.read_mj()
+        secs = g0.elapsed_time(g1) * 1e-3
+        if e_start is not None and e_end is not None and e_end > e_start:
+            joules = (e_end - e_start) * 1e-3
+            energy = {"joules_per_step": joules / n_en, "tflop_per_joule": flops * n_en / joules / 1e12,
+                      "avg_power_w": joules / secs, "steps": n_en, "seconds": secs,
+                      "method": "NVML total-energy counter (board), read before and after the loop"}
+        else:
+            energy = {"unavailable": "NVML energy counter not readable on this box"}
+
     # the Hadamard pre-pass of Q and K (bf16 -> rotated e4m3 + descale), timed on its own
     prepass = None
     if args.hadamard:
@@ -384,6 +441,8 @@ def main():
             line["e2e"] = e2e
         if prepass is not None:
             line["hadamard_prepass"] = prepass
+        if energy is not None:
+            line["energy"] = energy
         if not args.no_cpu and world == 1:
             line["cpu_baseline"] = cpu_oracle_sample(p, args.dtype, args.cpu_seconds)
         print(json.dumps(line), flush=True)
