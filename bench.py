@@ -172,6 +172,22 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def slowest_rank_ms(local_ms: float, world: int, device) -> float:
+    """The step time of the job: the maximum over ranks of each rank's own CUDA-event time."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica, so the work adds up over ranks and the
+    slowest rank's time is the job's time."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 def cpu_oracle_sample(p, dtype, budget_s):
     """Time the oracle on a seeded sample of query rows of the workload (rows are independent)."""
     import numpy as np
@@ -302,11 +318,8 @@ def main():
     clocks = sampler.stop() if rank == 0 else None
     total_ms = starts[0].elapsed_time(ends[-1])
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_per_step = float(t.item()) / args.steps
-    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    ms_per_step = slowest_rank_ms(total_ms, world, dev) / args.steps
+    value = job_throughput(flops, world, ms_per_step)
     zst = api.zyfa_check_errors(sptr)
     if zst != 0:
         raise api.ZyfaError(zst, "kernel status")
@@ -396,11 +409,9 @@ def main():
             hout.copy_(out, non_blocking=True)
         e1.record(stream)
         barrier()
-        te = torch.tensor([e0.elapsed_time(e1) / n_e2e], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": flops * world / (float(te.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": float(te.item()),
+        te = slowest_rank_ms(e0.elapsed_time(e1) / n_e2e, world, dev)
+        e2e = {"value": job_throughput(flops, world, te), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": te,
                "steps": n_e2e}
 
     if rank == 0:
