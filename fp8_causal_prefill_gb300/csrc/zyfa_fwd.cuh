@@ -488,7 +488,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // PV_t(j), announced on pv_done.  A K/V stage is released after the later of its (at most
         // two) PVs.
         auto do_pv = [&](int t, int j) {
-          const int nt = t ? n1 : n0;
           const uint32_t st = (kv_cnt + j) % C::kStages;
           issue_pv(t, st, j == 0);
           if (leader) tc_commit(smem_u32(&ctl.pv_done[t]));
@@ -517,6 +516,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         // belongs to the other query tile, before it when it belongs to the same one (so a score tile
         // always follows the previous PV of its own query tile) or when the K/V ring is short
         for (int j = 0; j < nkv && ok; ++j) {
+          if (!C::kScoreFirst && j >= 1 && j < n0 && n1 > 0) {
+            // steady state, short K/V ring: PV1(j-2), S0(j), PV0(j-1), S1(j) (each PV ahead of the
+            // score MMA, since that score MMA may need the stage the PV releases)
+            const uint32_t st = (kv_cnt + j) % C::kStages;
+            if (!(ok = mbar_wait(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit))) break;
+            tc_fence_after();
+            if (j >= 2) {
+              const uint32_t st2 = (kv_cnt + j - 2) % C::kStages;
+              issue_pv(1, st2, j == 2);
+              if (leader) {
+                tc_commit(smem_u32(&ctl.pv_done[1]));
+                tc_commit(smem_u32(&ctl.kv_empty[st2]));
+              }
+            }
+            if (!(ok = mbar_wait(smem_u32(&ctl.kv_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag,
+                                 kWaitLimit)))
+              break;
+            tc_fence_after();
+            issue_s(0, st);
+            if (leader && j == n0 - 1) tc_commit(smem_u32(&ctl.q_empty[0]));
+            if (!(ok = mbar_wait(smem_u32(&ctl.s_free), s_seq & 1, abort_flag, kWaitLimit))) break;
+            tc_fence_after();
+            const uint32_t st1 = (kv_cnt + j - 1) % C::kStages;
+            issue_pv(0, st1, j == 1);
+            if (leader) tc_commit(smem_u32(&ctl.pv_done[0]));
+            issue_s(1, st);
+            s_seq += 2;
+            last_t = 1;
+            last_j = j;
+            read_pending = true;
+            continue;
+          }
           if (C::kScoreFirst && j >= 1 && j < n0 && n1 > 0) {
             // steady state (both query tiles active): S0(j), PV1(j-2), S1(j), PV0(j-1)
             const uint32_t st = (kv_cnt + j) % C::kStages;
