@@ -21,7 +21,8 @@ ZYFA_DTYPE_E4M3 = 0
 ZYFA_DTYPE_BF16 = 1
 STATUS = {0: "ZYFA_OK", 1: "ZYFA_ERR_INVALID_ARG", 2: "ZYFA_ERR_UNSUPPORTED", 3: "ZYFA_ERR_MISALIGNED",
           4: "ZYFA_ERR_CUDA", 5: "ZYFA_ERR_TIMEOUT"}
-EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_attn_fwd_causal_ex", "zyfa_check_errors", "zyfa_status_string",
+EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_attn_fwd_causal_ex", "zyfa_attn_fwd_causal_host", "zyfa_check_errors",
+            "zyfa_status_string",
             "zyfa_kernel_launches", "zyfa_selftest_stalled_pipeline", "zyfa_hadamard_quantize_e4m3",
             "zyfa_hadamard_quantize_e4m3_noalloc", "zyfa_hadamard_workspace_bytes")
 ZYFA_P_LEAN = 0
@@ -58,6 +59,9 @@ def load_library() -> ctypes.CDLL:
         lib.zyfa_attn_fwd_causal_ex.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, vp, vp,
                                                 ctypes.POINTER(FwdOptions), vp]
         lib.zyfa_attn_fwd_causal_ex.restype = ci
+        lib.zyfa_attn_fwd_causal_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci,
+                                                  vp, vp, vp, ci, vp]
+        lib.zyfa_attn_fwd_causal_host.restype = ci
         lib.zyfa_selftest_stalled_pipeline.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, vp]
         lib.zyfa_selftest_stalled_pipeline.restype = ci
         ll, sz = ctypes.c_longlong, ctypes.c_size_t
@@ -96,6 +100,17 @@ def zyfa_attn_fwd_causal_ex(q: int, k: int, v: int, out: int, B: int, S: int, H:
     return lib.zyfa_attn_fwd_causal_ex(q, k, v, out, B, S, H, H_kv, D_qk, D_v, float(softmax_scale), dtype,
                                        q_descale or None, k_descale or None, v_descale or None,
                                        ctypes.byref(opts), stream or None)
+
+
+def zyfa_attn_fwd_causal_host(q_host: int, k_host: int, v_host: int, out_host: int, q_dev: int, k_dev: int,
+                              v_dev: int, out_dev: int, B: int, S: int, H: int, H_kv: int, D_qk: int, D_v: int,
+                              softmax_scale: float, dtype: int, q_descale: int = 0, k_descale: int = 0,
+                              v_descale: int = 0, chunks: int = 0, stream: int = 0) -> int:
+    """Call the host-buffer C entry point (transfers overlapped with compute); returns the status code."""
+    return load_library().zyfa_attn_fwd_causal_host(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev, out_dev,
+                                                    B, S, H, H_kv, D_qk, D_v, float(softmax_scale), dtype,
+                                                    q_descale or None, k_descale or None, v_descale or None,
+                                                    chunks, stream or None)
 
 
 def zyfa_selftest_stalled_pipeline(q: int, k: int, v: int, out: int, B: int, S: int, H: int, H_kv: int, D_qk: int,

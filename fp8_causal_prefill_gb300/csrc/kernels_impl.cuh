@@ -28,6 +28,7 @@ cudaError_t launch_fwd(const LaunchArgs& a) {
   p.H_kv = a.H_kv;
   p.softmax_scale = a.softmax_scale;
   p.num_units = a.num_units;
+  p.qb_end = a.qb_end;
   p.status = a.status;
   p.stall_loads = a.stall_loads;
   p.lse = a.lse;

@@ -18,6 +18,7 @@ struct LaunchArgs {
   int B, S, H, H_kv;
   float softmax_scale;
   int num_units;
+  int qb_end;  // last query block (exclusive) of the processed range
   int* status;
   int stall_loads;    // nonzero only for the stalled-pipeline self-test
   float* lse;         // optional log-sum-exp output [B,H,S]

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -36,6 +37,43 @@ bool get_encode() {
 
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int*> g_status_ptr[kMaxDevices];
+
+// Copy streams of the host-buffer entry point, one pair per device, created on first use and kept
+// for the life of the process (uploads and downloads run beside the caller's compute stream).
+constexpr int kMaxHostChunks = 64;
+std::mutex g_stream_mutex;
+cudaStream_t g_up[kMaxDevices], g_down[kMaxDevices];
+
+bool copy_streams(int dev, cudaStream_t* up, cudaStream_t* down) {
+  std::lock_guard<std::mutex> lock(g_stream_mutex);
+  if (!g_up[dev]) {
+    cudaStream_t a = nullptr, b = nullptr;
+    if (cudaStreamCreateWithFlags(&a, cudaStreamNonBlocking) != cudaSuccess) return false;
+    if (cudaStreamCreateWithFlags(&b, cudaStreamNonBlocking) != cudaSuccess) {
+      cudaStreamDestroy(a);
+      return false;
+    }
+    g_up[dev] = a;
+    g_down[dev] = b;
+  }
+  *up = g_up[dev];
+  *down = g_down[dev];
+  return true;
+}
+
+// Events of one host-buffer call; destroying a recorded event is safe (its resources go once it fired).
+struct EventSet {
+  cudaEvent_t e[2 * kMaxHostChunks + 2] = {};
+  int n = 0;
+  bool create(int count) {
+    for (; n < count; ++n)
+      if (cudaEventCreateWithFlags(&e[n], cudaEventDisableTiming) != cudaSuccess) return false;
+    return true;
+  }
+  ~EventSet() {
+    for (int i = 0; i < n; ++i) cudaEventDestroy(e[i]);
+  }
+};
 
 // Device-side address of the status word for the current device (looked up once per device).
 int* status_ptr(int dev) {
@@ -125,7 +163,7 @@ namespace {
 zyfa_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int S, int H, int H_kv,
                        int D_qk, int D_v, float softmax_scale, zyfa_dtype_t dtype, const float* q_descale,
                        const float* k_descale, const float* v_descale, const zyfa_fwd_options_t* opts,
-                       cudaStream_t stream, int stall_loads) {
+                       cudaStream_t stream, int stall_loads, long long qb_begin = 0, long long qb_end = -1) {
   if (B < 1 || H < 1 || H_kv < 1 || S < 0 || H % H_kv != 0) return ZYFA_ERR_INVALID_ARG;
   if (dtype != ZYFA_DTYPE_E4M3 && dtype != ZYFA_DTYPE_BF16) return ZYFA_ERR_INVALID_ARG;
   zyfa_fwd_options_t o = {ZYFA_P_LEAN, 0, nullptr};
@@ -141,8 +179,10 @@ zyfa_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, i
   auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out)) return ZYFA_ERR_MISALIGNED;
   const long long nqb = (static_cast<long long>(S) + kUnitRows - 1) / kUnitRows;
-  const long long units = nqb * B * H;
-  if (units > (1ll << 30) || static_cast<long long>(S) > (1ll << 30)) return ZYFA_ERR_UNSUPPORTED;
+  if (nqb * B * H > (1ll << 30) || static_cast<long long>(S) > (1ll << 30)) return ZYFA_ERR_UNSUPPORTED;
+  if (qb_end < 0) qb_end = nqb;
+  if (qb_begin < 0 || qb_begin >= qb_end || qb_end > nqb) return ZYFA_ERR_INVALID_ARG;
+  const long long units = (qb_end - qb_begin) * B * H;
   if (softmax_scale == 0.0f) softmax_scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D_qk)));
   if (!get_encode()) return ZYFA_ERR_CUDA;
 
@@ -165,6 +205,7 @@ zyfa_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, i
   a.H_kv = H_kv;
   a.softmax_scale = softmax_scale;
   a.num_units = static_cast<int>(units);
+  a.qb_end = static_cast<int>(qb_end);
   a.status = status;
   a.grid = static_cast<int>(units < nsm ? units : nsm);
   a.stream = stream;
@@ -204,6 +245,62 @@ zyfa_status_t zyfa_attn_fwd_causal_ex(const void* q, const void* k, const void* 
                                       const zyfa_fwd_options_t* options, cudaStream_t stream) {
   return attn_fwd(q, k, v, out, B, S, H, H_kv, D_qk, D_v, softmax_scale, dtype, q_descale, k_descale, v_descale,
                   options, stream, 0);
+}
+
+zyfa_status_t zyfa_attn_fwd_causal_host(const void* q_host, const void* k_host, const void* v_host, void* out_host,
+                                        void* q_dev, void* k_dev, void* v_dev, void* out_dev, int B, int S, int H,
+                                        int H_kv, int D_qk, int D_v, float softmax_scale, zyfa_dtype_t dtype,
+                                        const float* q_descale, const float* k_descale, const float* v_descale,
+                                        int chunks, cudaStream_t stream) {
+  if (B < 1 || H < 1 || H_kv < 1 || S < 0 || H % H_kv != 0 || chunks < 0) return ZYFA_ERR_INVALID_ARG;
+  if (dtype != ZYFA_DTYPE_E4M3 && dtype != ZYFA_DTYPE_BF16) return ZYFA_ERR_INVALID_ARG;
+  const bool shape_ok = (D_qk == 64 && D_v == 64) || (D_qk == 128 && D_v == 128) || (D_qk == 192 && D_v == 128);
+  if (!shape_ok) return ZYFA_ERR_UNSUPPORTED;
+  if (S == 0) return ZYFA_OK;
+  if (!q_host || !k_host || !v_host || !out_host) return ZYFA_ERR_INVALID_ARG;
+  const long long nqb = (static_cast<long long>(S) + kUnitRows - 1) / kUnitRows;
+  if (chunks == 0) chunks = 8;
+  if (chunks > nqb) chunks = static_cast<int>(nqb);
+  if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ZYFA_ERR_CUDA;
+  cudaStream_t up = nullptr, down = nullptr;
+  if (!copy_streams(dev, &up, &down)) return ZYFA_ERR_CUDA;
+
+  const size_t es = dtype == ZYFA_DTYPE_E4M3 ? 1 : 2;
+  const size_t row_q = static_cast<size_t>(H) * D_qk * es, row_k = static_cast<size_t>(H_kv) * D_qk * es;
+  const size_t row_v = static_cast<size_t>(H_kv) * D_v * es, row_o = static_cast<size_t>(H) * D_v * 2;
+  // rows [r0, r1) of every batch of a [B][S][row] tensor: one pitched copy of B pieces
+  auto copy_rows = [&](void* dst, const void* src, size_t row, long long r0, long long r1, cudaMemcpyKind kind,
+                       cudaStream_t st) {
+    const size_t off = static_cast<size_t>(r0) * row, pitch = static_cast<size_t>(S) * row;
+    return cudaMemcpy2DAsync(static_cast<char*>(dst) + off, pitch, static_cast<const char*>(src) + off, pitch,
+                             static_cast<size_t>(r1 - r0) * row, static_cast<size_t>(B), kind, st) == cudaSuccess;
+  };
+  EventSet ev;
+  if (!ev.create(2 * chunks + 2)) return ZYFA_ERR_CUDA;
+  bool ok = cudaEventRecord(ev.e[0], stream) == cudaSuccess && cudaStreamWaitEvent(up, ev.e[0], 0) == cudaSuccess;
+  zyfa_status_t st = ZYFA_OK;
+  for (int c = 0; ok && c < chunks; ++c) {
+    const long long qb0 = nqb * c / chunks, qb1 = nqb * (c + 1) / chunks;
+    const long long r0 = qb0 * kUnitRows, r1 = std::min<long long>(qb1 * kUnitRows, S);
+    ok = copy_rows(q_dev, q_host, row_q, r0, r1, cudaMemcpyHostToDevice, up) &&
+         copy_rows(k_dev, k_host, row_k, r0, r1, cudaMemcpyHostToDevice, up) &&
+         copy_rows(v_dev, v_host, row_v, r0, r1, cudaMemcpyHostToDevice, up) &&
+         cudaEventRecord(ev.e[1 + 2 * c], up) == cudaSuccess && cudaStreamWaitEvent(stream, ev.e[1 + 2 * c], 0) == cudaSuccess;
+    if (!ok) break;
+    // query blocks [qb0, qb1) read keys [0, r1): every one of them arrived with this or an earlier chunk
+    st = attn_fwd(q_dev, k_dev, v_dev, out_dev, B, S, H, H_kv, D_qk, D_v, softmax_scale, dtype, q_descale, k_descale,
+                  v_descale, nullptr, stream, 0, qb0, qb1);
+    if (st != ZYFA_OK) break;
+    ok = cudaEventRecord(ev.e[2 + 2 * c], stream) == cudaSuccess && cudaStreamWaitEvent(down, ev.e[2 + 2 * c], 0) == cudaSuccess &&
+         copy_rows(out_host, out_dev, row_o, r0, r1, cudaMemcpyDeviceToHost, down);
+  }
+  // the caller's stream resumes once the last output rows are back on the host
+  const bool tail = cudaEventRecord(ev.e[2 * chunks + 1], down) == cudaSuccess &&
+                    cudaStreamWaitEvent(stream, ev.e[2 * chunks + 1], 0) == cudaSuccess;
+  if (st != ZYFA_OK) return st;
+  return ok && tail ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
 zyfa_status_t zyfa_selftest_stalled_pipeline(const void* q, const void* k, const void* v, void* out, int B, int S,

@@ -128,7 +128,8 @@ struct Params {
   const float* v_descale;
   int B, S, H, H_kv;
   float softmax_scale;
-  int num_units;  // B*H*ceil(S/256)
+  int num_units;  // B*H*(qb_end - qb_begin)
+  int qb_end;     // query blocks (256 rows) [qb_end - num_units/(B*H), qb_end) are processed
   int* status;    // device status word (timeouts)
   int stall_loads;  // self-test of the timeout path: the producer withholds every load
   float* lse;       // optional [B,H,S] natural-log sum of exp of the scores (nullptr: not written)
@@ -157,8 +158,7 @@ __device__ __forceinline__ bool unit_at(const Params& p, int round, Unit& u) {
   const int idx = round * G + ((round & 1) ? (G - 1 - c) : c);
   if (idx >= p.num_units) return false;
   const int bh = p.B * p.H;
-  const int nqb = (p.S + kUnitRows - 1) / kUnitRows;
-  const int qb = nqb - 1 - idx / bh;
+  const int qb = p.qb_end - 1 - idx / bh;
   const int rest = idx % bh;
   u.b = rest / p.H;
   u.h = rest % p.H;

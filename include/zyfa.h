@@ -107,6 +107,36 @@ zyfa_status_t zyfa_attn_fwd_causal_ex(const void* q, const void* k, const void* 
                                       cudaStream_t stream);
 
 /*
+ * zyfa_attn_fwd_causal_host - zyfa_attn_fwd_causal for inputs and output in host memory, with the
+ * transfers overlapped with the computation.
+ *
+ * The query rows are split into `chunks` groups of 256-row blocks (0 = 8; at most 64 and at most one
+ * per block).  Chunk c's rows of q, k and v are copied to the device buffers on an internal upload
+ * stream; the kernel for chunk c's query rows then runs on `stream` (causality: those rows read keys
+ * and values of chunks <= c only, all already uploaded); its output rows are copied back on an
+ * internal download stream while later chunks compute.  `stream` waits for the last download, so
+ * synchronising `stream` (or a later operation on it) sees the complete output in `out_host`.
+ *
+ *   q_host, k_host, v_host   host memory, layout as for zyfa_attn_fwd_causal; page-locked (pinned)
+ *                            memory is needed for the copies to overlap (pageable memory works but
+ *                            serialises them).  Read after earlier work on `stream`.
+ *   out_host                 host memory [B,S,H,D_v] bf16, written by the call.
+ *   q_dev, k_dev, v_dev, out_dev
+ *                            device buffers of the full tensor sizes, 16-byte aligned, owned by the
+ *                            caller (they hold the uploaded inputs and the output afterwards).
+ *   q/k/v_descale            device pointers as for zyfa_attn_fwd_causal.
+ *   chunks, stream           see above.
+ * Other arguments and errors as zyfa_attn_fwd_causal (plus ZYFA_ERR_INVALID_ARG for null host
+ * pointers or chunks < 0).  The two copy streams are created on the first call on a device and kept
+ * for the life of the process; the call allocates no memory.
+ */
+zyfa_status_t zyfa_attn_fwd_causal_host(const void* q_host, const void* k_host, const void* v_host, void* out_host,
+                                        void* q_dev, void* k_dev, void* v_dev, void* out_dev, int B, int S, int H,
+                                        int H_kv, int D_qk, int D_v, float softmax_scale, zyfa_dtype_t dtype,
+                                        const float* q_descale, const float* k_descale, const float* v_descale,
+                                        int chunks, cudaStream_t stream);
+
+/*
  * zyfa_hadamard_quantize_e4m3 - Hadamard rotation and per-tensor FP8 quantisation of Q or K, the
  * pre-pass that roughly halves the error input quantisation adds to attention (spbcomputers.ru ZYFA
  * article, FAQ "Что даёт поворот Адамара?"; captivela ZYFA article, "Angka Nyata").  Rotating Q and K
