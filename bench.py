@@ -418,7 +418,7 @@ def main():
         te = slowest_rank_ms(e0.elapsed_time(e1) / n_e2e, world, dev)
         e2e = {"value": job_throughput(flops, world, te), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": te,
-               "steps": n_e2e, "call": "zyfa_attn_fwd_causal_host (pinned host buffers, 8 chunks)"}
+               "steps": n_e2e, "call": "zyfa_attn_fwd_causal_host (pinned host buffers, 4 chunks)"}
 
     if rank == 0:
         peaks, src = load_peaks()

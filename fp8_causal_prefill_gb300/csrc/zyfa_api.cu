@@ -259,7 +259,7 @@ zyfa_status_t zyfa_attn_fwd_causal_host(const void* q_host, const void* k_host, 
   if (S == 0) return ZYFA_OK;
   if (!q_host || !k_host || !v_host || !out_host) return ZYFA_ERR_INVALID_ARG;
   const long long nqb = (static_cast<long long>(S) + kUnitRows - 1) / kUnitRows;
-  if (chunks == 0) chunks = 8;
+  if (chunks == 0) chunks = 4;
   if (chunks > nqb) chunks = static_cast<int>(nqb);
   if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;
   int dev = 0;
