@@ -216,7 +216,8 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t a) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// tcgen05.mma (issued by one thread).  `acc` = 0 overwrites D, 1 accumulates into D.
+// tcgen05.mma (a single-thread instruction: callers issue it from one elected lane).  `acc` = 0
+// overwrites D, 1 accumulates into D.
 
 // D(tmem) = A(smem) x B(smem)
 __device__ __forceinline__ void mma_f8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,

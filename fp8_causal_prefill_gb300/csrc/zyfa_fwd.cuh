@@ -17,13 +17,13 @@
 // rounded p (accumulated by the softmax threads), no block scaling.
 //
 // Schedule (one persistent CTA per SM; one work unit = (b, h, 256 query rows) = two 128-row tiles
-// Q0, Q1 that share every K/V tile of BN keys):
+// Q0, Q1 that share every K/V tile of BN keys; a launch covers the query blocks of a given range):
 //   warp 0      TMA producer: Q tiles and a ring of K/V stages in shared memory
 //   warp 1      MMA issuer (the whole warp runs the loop, one elected lane issues) and TMEM owner
 //   warps 4..7  softmax warpgroup of Q0, warps 8..11 softmax warpgroup of Q1
 // The two score tiles share one TMEM buffer, filled in the order S0(0), S1(0), S0(1), S1(1), ...: a
 // softmax warpgroup copies its scores to registers and releases the buffer at once, and the next
-// score MMA is issued as soon as that release is seen.  The release also tells the MMA thread that
+// score MMA is issued as soon as that release is seen.  The release also tells the MMA warp that
 // the warpgroup's previous P is in TMEM, so PV_t(j-1) is issued right after the score MMA that follows
 // the read of S_t(j): score MMAs never wait for a softmax computation, and the PV of one tile keeps
 // the tensor core busy while the other tile's scores are handed over (the pages' ping-pong, here
@@ -31,13 +31,13 @@
 // pv_done barrier; a warpgroup stores P_t(j) (and rescales O_t) once PV_t(j-1) has completed.
 // The MMA warp's own instruction stream is on the critical path, so the middle of every unit (both
 // query tiles active) runs as a fixed, branch-free sequence.
-// Every tcgen05 instruction costs the issuing thread tens of cycles, so score MMAs are 128 keys wide.
+// Every tcgen05 instruction costs the issuing warp tens of cycles, so score MMAs are 128 keys wide.
 //
 // Tensor memory (512 columns x 128 lanes; lane = query row of a tile):
 //   [  0,128)            S: fp32 scores of the tile being handed to a softmax warpgroup
 //   [128,128+NO)         O0 (fp32, DV output columns; FP8: then 16 columns of the rounded row sum)
 //   [128+NO,128+2NO)     O1
-//   [416,480)            P tiles (FP8: P0 | P1, e4m3 codes, BN/4 columns each; BF16: one shared tile)
+//   [416,480)            FP8: P0 | P1, e4m3 codes, BN/4 columns each;  BF16: [384,448) P0, [448,512) P1
 //   [480,484) [488,492)  e8m0 scale factors of P0, P1 (FP8)   [496,504) scale factors of V (all 1.0)
 #pragma once
 #include <cstdint>
