@@ -22,6 +22,11 @@
  *     out [B, S, H,    D_v ]   bf16, written in full for every call with S > 0
  * Supported head shapes (D_qk, D_v): (64, 64), (128, 128), (192, 128) (the last one is the
  * DeepSeek-style multi-head latent attention shape, 128 "nope" + 64 rotary dims).
+ * Inputs must be finite (no e4m3 NaN codes 0x7F / 0xFF, no bf16 Inf or NaN); the output for
+ * non-finite inputs is unspecified.  A 64-key block whose scale lies more than 127 binades below its
+ * row's reference contributes at most 2^-127 of its weight (its E8M0 scale is clamped).  FP8 scaled
+ * scores (softmax_scale * descales * q.k) must stay below 2^16 binades in magnitude, where the
+ * Lean-P offset 55.625 - 8e is still exact in fp32 (attention scores are many orders smaller).
  */
 #ifndef ZYFA_H_
 #define ZYFA_H_

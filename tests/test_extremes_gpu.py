@@ -1,0 +1,48 @@
+"""Edge cases at the extremes: a sequence four times the bench length, and score ranges so wide that
+whole 64-key blocks fall more than 127 binades below the row's reference (their E8M0 scale leaves the
+representable range; the method's weights there are below 2^-127 of the row's largest and vanish)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from _gpu_util import FP8_TOL, oracle_out, per_row_rel, select, to_device
+from fp8_causal_prefill_gb300 import flash_attn_func, zyfa_check_errors
+from fp8_causal_prefill_gb300.inputs import Shape, make_problem, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def test_sequence_of_128k_tokens_sampled_rows():
+    sh = Shape(1, 131072, 2, 1, 128, 128)
+    p = make_problem(sh, seed=31, bf16=False)
+    q, k, v, ds = to_device(p, "fp8")
+    out = flash_attn_func(q, k, v, q_descale=ds[0], k_descale=ds[1], v_descale=ds[2])
+    torch.cuda.synchronize()
+    assert zyfa_check_errors() == 0
+    rows = sample_rows(sh.S, n_random=96, edge=32, seed=4)
+    got = select(out, rows=rows)
+    ref = oracle_out(p, "fp8", rows=rows)
+    assert O.rel_l2(got, ref) <= FP8_TOL
+    assert per_row_rel(got, ref).max() <= 5e-2
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("p_mode", ["lean", "exact"])
+def test_extreme_score_range(p_mode):
+    # the same codes with q/k descales 10x larger: score spreads of ~800 binades per row (up to ~700
+    # binades from zero), so many blocks sit more than 127 binades below the row maximum (weight 0 in
+    # the oracle, at most 2^-127 of it on the device) while the top blocks decide the output.  (The
+    # block exponents stay far inside the range where 55.625 - 8e is exact in fp32.)
+    sh = Shape(1, 700, 2, 1, 128, 128)
+    p = make_problem(sh, seed=32, bf16=False)
+    p.dq, p.dk = p.dq * 10.0, p.dk * 10.0
+    q, k, v, ds = to_device(p, "fp8")
+    out = flash_attn_func(q, k, v, q_descale=ds[0], k_descale=ds[1], v_descale=ds[2], p_mode=p_mode)
+    torch.cuda.synchronize()
+    assert zyfa_check_errors() == 0
+    f = O.exactp_causal_attention if p_mode == "exact" else O.leanp_causal_attention
+    ref = f(p.q8.numpy(), p.k8.numpy(), p.v8.numpy(), p.dq, p.dk, p.dv, O.default_softmax_scale(128))
+    got = select(out)
+    assert np.all(np.isfinite(got))
+    assert O.rel_l2(got, ref) <= FP8_TOL
