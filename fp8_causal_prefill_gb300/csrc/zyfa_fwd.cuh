@@ -18,8 +18,10 @@
 //
 // Schedule (one persistent CTA per SM; one work unit = (b, h, 256 query rows) = two 128-row tiles
 // Q0, Q1 that share every K/V tile of BN keys; a launch covers the query blocks of a given range):
-//   warp 0      TMA producer: Q tiles and a ring of K/V stages in shared memory
+//   warp 0      TMA producer: Q tiles and K tiles (and V tiles, when K and V share one ring)
 //   warp 1      MMA issuer (the whole warp runs the loop, one elected lane issues) and TMEM owner
+//   warp 2      TMA producer of V tiles when K and V have rings of their own (three slots or fewer:
+//               BF16 at D=128, both types at D=192)
 //   warps 4..7  softmax warpgroup of Q0, warps 8..11 softmax warpgroup of Q1
 // The two score tiles share one TMEM buffer, filled in the order S0(0), S1(0), S0(1), S1(1), ...: a
 // softmax warpgroup copies its scores to registers and releases the buffer at once, and the next
@@ -111,13 +113,15 @@ struct Cfg {
   static constexpr uint32_t kColSFB = 496;
   static_assert(128 + 2 * kNO <= static_cast<int>(kColP), "O accumulators overlap the P tiles");
   static_assert(kColP + 2 * kPCols <= (FP8 ? 480u : 512u), "P tiles overlap the scale factors");
-  // Issue order after a score tile is seen read: with three or more K/V stages the next score MMA
-  // goes first (it gates a softmax warpgroup); with two, the PV goes first, because the next score
-  // MMA may need the stage that PV releases.
-  static constexpr bool kScoreFirst = kStages >= 3;
-  // The last PV of query tile 0 waits for the end of the unit, while tile 1 may still need up to
-  // kBlockM / BN more K/V tiles: the ring must hold them without that PV's stage.
-  static_assert(kStages > kBlockM / BN, "K/V ring too short for the PV lag");
+  // K and V tiles sit in two rings of kStages slots.  With a short ring (three slots or fewer) K and V
+  // have their own barriers and producers: a K slot is free once the last score MMA of its tile
+  // completed, a V slot once the last PV did, so a score MMA never waits for a PV.  A longer ring
+  // (whose stages are always ready in time) keeps one barrier per K/V pair, released after the later
+  // PV, which spares the MMA warp a wait and a commit per tile.
+  static constexpr bool kSplitKV = kStages <= 3;
+  // With one barrier per K/V pair, the last PV of query tile 0 waits for the end of the unit while
+  // tile 1 may still need up to kBlockM / BN more tiles: the ring must hold them.
+  static_assert(kSplitKV || kStages > kBlockM / BN, "K/V ring too short for the PV lag");
   static_assert(kNO % 16 == 0 && kNO <= 256, "PV MMA width");
 };
 
@@ -137,7 +141,7 @@ struct Params {
 };
 
 struct __align__(8) SharedCtl {
-  uint64_t kv_full[8], kv_empty[8];
+  uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
   uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], pv_done[2];
   uint64_t s_free, drain;
   uint32_t tmem_base;
@@ -300,14 +304,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_stages = s_q + 2 * C::kQTileBytes;
   // FP8: one atom of e4m3 1.0 above every V stage; the PV descriptor reaches it through its
   // leading-dimension offset (a positive distance from each stage)
+  // split rings: all K slots, then all V slots; one ring: each slot holds a K tile and its V tile
   const uint32_t s_ones = s_stages + C::kStages * C::kStageBytes;
-  auto k_stage = [&](int s) { return s_stages + s * C::kStageBytes; };
-  auto v_stage = [&](int s) { return s_stages + s * C::kStageBytes + C::kKStageBytes; };
+  auto k_stage = [&](int s) { return s_stages + s * (C::kSplitKV ? C::kKStageBytes : C::kStageBytes); };
+  auto v_stage = [&](int s) {
+    return C::kSplitKV ? s_stages + C::kStages * C::kKStageBytes + s * C::kVStageBytes
+                       : s_stages + s * C::kStageBytes + C::kKStageBytes;
+  };
 
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(smem_u32(&ctl.kv_full[s]), 1);
-      mbar_init(smem_u32(&ctl.kv_empty[s]), 1);
+      mbar_init(smem_u32(&ctl.k_full[s]), 1);
+      mbar_init(smem_u32(&ctl.k_empty[s]), 1);
+      mbar_init(smem_u32(&ctl.v_full[s]), 1);
+      mbar_init(smem_u32(&ctl.v_empty[s]), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&ctl.q_full[t]), 1);
@@ -342,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hgroup = p.H / p.H_kv;
 
   if (warp == 0) {
-    // =========================== TMA producer ===========================
+    // =========================== TMA producer: Q and K (and V with a long ring) ===========================
     regs_dec<kRegsControl>();
     if (!p.stall_loads) {
       const bool leader = elect_one();
@@ -378,19 +388,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; j < nkv && ok; ++j) {
           const int st = kv_cnt % C::kStages;
-          ok = mbar_wait(smem_u32(&ctl.kv_empty[st]), ((kv_cnt / C::kStages) & 1) ^ 1, abort_flag, kWaitLimit);
+          ok = mbar_wait(smem_u32(&ctl.k_empty[st]), ((kv_cnt / C::kStages) & 1) ^ 1, abort_flag, kWaitLimit);
           if (!ok) break;
-          const uint32_t bar = smem_u32(&ctl.kv_full[st]);
+          const uint32_t bar = smem_u32(&ctl.k_full[st]);
           if (leader) {
-            mbar_arrive_expect_tx(bar, C::kKStageBytes + C::kVStageBytes);
+            mbar_arrive_expect_tx(bar, C::kKStageBytes + (C::kSplitKV ? 0 : C::kVStageBytes));
             for (int c = 0; c < C::kChunks128K; ++c)
               tma_load_4d(k_stage(st) + c * (BN * 128), &maps.k0, bar, c * (128 / C::kElem), hk, j * BN, u.b);
             if (C::kTail64K)
               tma_load_4d(k_stage(st) + C::kChunks128K * (BN * 128), &maps.k1, bar,
                           C::kChunks128K * (128 / C::kElem), hk, j * BN, u.b);
-            for (int c = 0; c < C::kVAtoms; ++c)
-              tma_load_4d(v_stage(st) + c * C::kVAtomBytes, &maps.v, bar, c * (C::kVAtomRow / C::kElem), hk,
-                          j * BN, u.b);
+            if (!C::kSplitKV)  // V on the same barrier
+              for (int c = 0; c < C::kVAtoms; ++c)
+                tma_load_4d(v_stage(st) + c * C::kVAtomBytes, &maps.v, bar, c * (C::kVAtomRow / C::kElem), hk,
+                            j * BN, u.b);
           }
           ++kv_cnt;
         }
@@ -401,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int never = 0;
         const uint32_t ns = C::kStages;
         for (uint32_t i = (kv_cnt > ns ? kv_cnt - ns : 0); i < kv_cnt; ++i)
-          mbar_wait(smem_u32(&ctl.kv_full[i % ns]), (i / ns) & 1, &never, kWaitLimit);
+          mbar_wait(smem_u32(&ctl.k_full[i % ns]), (i / ns) & 1, &never, kWaitLimit);
         for (int t = 0; t < 2; ++t)
           if (q_cnt[t] > 0) mbar_wait(smem_u32(&ctl.q_full[t]), (q_cnt[t] - 1) & 1, &never, kWaitLimit);
       }
@@ -419,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t q_tail0 = smem_desc(s_q + C::kChunks128K * (kBlockM * 128), 16, 512, kSwizzle64B);
       const uint64_t k_desc0 = smem_desc(k_stage(0), 16, 1024, kSwizzle128B);
       const uint64_t k_tail0 = smem_desc(k_stage(0) + C::kChunks128K * (BN * 128), 16, 512, kSwizzle64B);
-      constexpr uint32_t kQTile16 = C::kQTileBytes >> 4, kStage16 = C::kStageBytes >> 4;
+      constexpr uint32_t kQTile16 = C::kQTileBytes >> 4, kStage16 = (C::kSplitKV ? C::kKStageBytes : C::kStageBytes) >> 4;
       uint32_t kv_cnt = 0, s_seq = 0;
       uint32_t q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
       bool ok = true;
@@ -487,12 +498,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // PV_t(j), announced on pv_done.  A K/V stage is released after the later of its (at most
         // two) PVs.
-        auto do_pv = [&](int t, int j) {
+        auto do_pv = [&](int t, int j) -> bool {
           const uint32_t st = (kv_cnt + j) % C::kStages;
+          if constexpr (C::kSplitKV) {
+            if (!mbar_wait(smem_u32(&ctl.v_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag, kWaitLimit))
+              return false;
+            tc_fence_after();
+          }
           issue_pv(t, st, j == 0);
           if (leader) tc_commit(smem_u32(&ctl.pv_done[t]));
           const bool pv0_last = n1 == 0 || (j == n0 - 1 && n1 > n0);
-          if (leader && (t == 0) == pv0_last) tc_commit(smem_u32(&ctl.kv_empty[st]));
+          if (leader && (t == 0) == pv0_last)
+            tc_commit(smem_u32(C::kSplitKV ? &ctl.v_empty[st] : &ctl.k_empty[st]));
+          return true;
         };
         // Waits until the last score tile issued has been copied out of the shared S buffer.  Its
         // reader stored P of its previous tile before that, so the PV of that tile may follow; that
@@ -514,45 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // score tiles in the order S0(0), S1(0), S0(1), S1(1), ...; each one waits until the previous
         // was read, and the PV that read unlocks is issued next to it: after the score MMA when that
         // belongs to the other query tile, before it when it belongs to the same one (so a score tile
-        // always follows the previous PV of its own query tile) or when the K/V ring is short
+        // always follows the previous PV of its own query tile)
         for (int j = 0; j < nkv && ok; ++j) {
-          if (!C::kScoreFirst && j >= 1 && j < n0 && n1 > 0) {
-            // steady state, short K/V ring: PV1(j-2), S0(j), PV0(j-1), S1(j) (each PV ahead of the
-            // score MMA, since that score MMA may need the stage the PV releases)
-            const uint32_t st = (kv_cnt + j) % C::kStages;
-            if (!(ok = mbar_wait(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit))) break;
-            tc_fence_after();
-            if (j >= 2) {
-              const uint32_t st2 = (kv_cnt + j - 2) % C::kStages;
-              issue_pv(1, st2, j == 2);
-              if (leader) {
-                tc_commit(smem_u32(&ctl.pv_done[1]));
-                tc_commit(smem_u32(&ctl.kv_empty[st2]));
-              }
-            }
-            if (!(ok = mbar_wait(smem_u32(&ctl.kv_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag,
-                                 kWaitLimit)))
-              break;
-            tc_fence_after();
-            issue_s(0, st);
-            if (leader && j == n0 - 1) tc_commit(smem_u32(&ctl.q_empty[0]));
-            if (!(ok = mbar_wait(smem_u32(&ctl.s_free), s_seq & 1, abort_flag, kWaitLimit))) break;
-            tc_fence_after();
-            const uint32_t st1 = (kv_cnt + j - 1) % C::kStages;
-            issue_pv(0, st1, j == 1);
-            if (leader) tc_commit(smem_u32(&ctl.pv_done[0]));
-            issue_s(1, st);
-            s_seq += 2;
-            last_t = 1;
-            last_j = j;
-            read_pending = true;
-            continue;
-          }
-          if (C::kScoreFirst && j >= 1 && j < n0 && n1 > 0) {
+          if (j >= 1 && j < n0 && n1 > 0) {
             // steady state (both query tiles active): S0(j), PV1(j-2), S1(j), PV0(j-1)
             const uint32_t st = (kv_cnt + j) % C::kStages;
             if (!(ok = mbar_wait(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit))) break;
-            if (!(ok = mbar_wait(smem_u32(&ctl.kv_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag,
+            if (!(ok = mbar_wait(smem_u32(&ctl.k_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag,
                                  kWaitLimit)))
               break;
             tc_fence_after();
@@ -560,16 +546,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader && j == n0 - 1) tc_commit(smem_u32(&ctl.q_empty[0]));
             if (j >= 2) {
               const uint32_t st2 = (kv_cnt + j - 2) % C::kStages;
+              if constexpr (C::kSplitKV) {
+                if (!(ok = mbar_wait(smem_u32(&ctl.v_full[st2]), ((kv_cnt + j - 2) / C::kStages) & 1, abort_flag,
+                                     kWaitLimit)))
+                  break;
+                tc_fence_after();
+              }
               issue_pv(1, st2, j == 2);
               if (leader) {
                 tc_commit(smem_u32(&ctl.pv_done[1]));
-                tc_commit(smem_u32(&ctl.kv_empty[st2]));
+                tc_commit(smem_u32(C::kSplitKV ? &ctl.v_empty[st2] : &ctl.k_empty[st2]));
               }
             }
             if (!(ok = mbar_wait(smem_u32(&ctl.s_free), s_seq & 1, abort_flag, kWaitLimit))) break;
             tc_fence_after();
             issue_s(1, st);
+            if (C::kSplitKV && leader) tc_commit(smem_u32(&ctl.k_empty[st]));  // S1(j): last reader of K tile j
             const uint32_t st1 = (kv_cnt + j - 1) % C::kStages;
+            if constexpr (C::kSplitKV) {
+              if (!(ok = mbar_wait(smem_u32(&ctl.v_full[st1]), ((kv_cnt + j - 1) / C::kStages) & 1, abort_flag,
+                                   kWaitLimit)))
+                break;
+              tc_fence_after();
+            }
             issue_pv(0, st1, j == 1);
             if (leader) tc_commit(smem_u32(&ctl.pv_done[0]));
             s_seq += 2;
@@ -582,10 +581,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < 2; ++t) {
             if (j >= (t ? n1 : n0)) continue;
             if (!(ok = wait_read())) break;
-            const bool pv_first = rj >= 0 && (rt == t || !C::kScoreFirst);
-            if (pv_first) do_pv(rt, rj);
-            if (t == 0 || j >= n0) {  // first score tile of K/V tile j
-              if (!(ok = mbar_wait(smem_u32(&ctl.kv_full[(kv_cnt + j) % C::kStages]),
+            // a PV of the same query tile goes before its next score MMA, one of the other tile after it
+            const bool pv_first = rj >= 0 && rt == t;
+            if (pv_first && !(ok = do_pv(rt, rj))) break;
+            if (t == 0 || j >= n0) {  // first score tile of K tile j
+              if (!(ok = mbar_wait(smem_u32(&ctl.k_full[(kv_cnt + j) % C::kStages]),
                                    ((kv_cnt + j) / C::kStages) & 1, abort_flag, kWaitLimit)))
                 break;
               tc_fence_after();
@@ -596,14 +596,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             last_t = t;
             last_j = j;
             if (leader && j == (t ? n1 : n0) - 1) tc_commit(smem_u32(&ctl.q_empty[t]));
-            if (rj >= 0 && !pv_first) do_pv(rt, rj);
+            // the last score MMA reading K tile j: S1(j), or S0(j) when query tile 1 has no tile j
+            if (C::kSplitKV && leader && (t == 1 || j >= n1))
+              tc_commit(smem_u32(&ctl.k_empty[(kv_cnt + j) % C::kStages]));
+            if (rj >= 0 && !pv_first && !(ok = do_pv(rt, rj))) break;
           }
         }
         if (!ok) break;
         // unit end: the read of the last score tile unlocks one more PV; the last PV of each query
         // tile waits for the softmax warpgroup's P directly
         if (!(ok = wait_read())) break;
-        if (rj >= 0) do_pv(rt, rj);
+        if (rj >= 0 && !(ok = do_pv(rt, rj))) break;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int nt = t ? n1 : n0;
@@ -611,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(smem_u32(&ctl.p_full[t]), p_cnt[t] & 1, abort_flag, kWaitLimit))) break;
           ++p_cnt[t];
           tc_fence_after();
-          do_pv(t, nt - 1);
+          if (!(ok = do_pv(t, nt - 1))) break;
         }
         kv_cnt += nkv;
       }
@@ -621,8 +624,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) tc_commit(smem_u32(&ctl.drain));
       mbar_wait(smem_u32(&ctl.drain), 0, &never, kWaitLimit);
     }
+  } else if (warp == 2) {
+    // =========================== TMA producer: V (short rings) ===========================
+    regs_dec<kRegsControl>();
+    if (C::kSplitKV && !p.stall_loads) {
+      const bool leader = elect_one();
+      uint32_t v_cnt = 0;
+      bool ok = true;
+      Unit u;
+      for (int round = 0; ok && unit_at(p, round, u); ++round) {
+        const int hk = u.h / hgroup;
+        const int n0 = tiles_for<BN>(p, u.r0, 0), n1 = tiles_for<BN>(p, u.r0, 1);
+        const int nkv = n1 > n0 ? n1 : n0;
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int st = v_cnt % C::kStages;
+          ok = mbar_wait(smem_u32(&ctl.v_empty[st]), ((v_cnt / C::kStages) & 1) ^ 1, abort_flag, kWaitLimit);
+          if (!ok) break;
+          const uint32_t bar = smem_u32(&ctl.v_full[st]);
+          if (leader) {
+            mbar_arrive_expect_tx(bar, C::kVStageBytes);
+            for (int c = 0; c < C::kVAtoms; ++c)
+              tma_load_4d(v_stage(st) + c * C::kVAtomBytes, &maps.v, bar, c * (C::kVAtomRow / C::kElem), hk,
+                          j * BN, u.b);
+          }
+          ++v_cnt;
+        }
+      }
+      if (!ok) {
+        if (leader) give_up();
+        const int never = 0;
+        const uint32_t ns = C::kStages;
+        for (uint32_t i = (v_cnt > ns ? v_cnt - ns : 0); i < v_cnt; ++i)
+          mbar_wait(smem_u32(&ctl.v_full[i % ns]), (i / ns) & 1, &never, kWaitLimit);
+      }
+    }
   } else if (warp < 4) {
-    regs_dec<kRegsControl>();  // warps 2, 3: idle members of the control warpgroup
+    regs_dec<kRegsControl>();  // warp 3: idle member of the control warpgroup
   } else {
     // =========================== softmax warpgroups ===========================
     regs_inc<kRegsSoftmax>();
