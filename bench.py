@@ -121,9 +121,10 @@ class EnergyCounter:
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms during the timed region."""
+    """nvidia-smi sampled every 50 ms; only samples stamped inside the timed region (host wall clock,
+    from the launch of the first timed step to the synchronize after the last) are summarised."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw.instant,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -131,13 +132,17 @@ class ClockSampler:
         self.dev = device_index
         self.proc = None
         self.path = None
+        self.window = None
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
 
     def start(self):
         fd, self.path = tempfile.mkstemp(prefix="zyfa_clocks_", suffix=".csv")
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -151,25 +156,33 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+        rows = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                vals = (float(parts[1]), float(parts[2]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+            try:
+                pw = float(parts[3])
+            except ValueError:
+                pw = None
+            rows.append((ts, vals[0], vals[1], pw, parts[5:9]))
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+        inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
+        used = inside if inside else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {n for r in used for n, v in zip(names, r[4]) if v.lower().startswith("active")}
+        sm = [r[1] for r in used]
+        power = [r[3] for r in used if r[3] is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_mhz_min": min(sm) if sm else None,
+                "sm_max_mhz": max(r[2] for r in used) if used else None,
                 "power_w_median": statistics.median(power) if power else None, "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "samples_in_window": bool(inside), "reasons": sorted(reasons)}
 
 
 def slowest_rank_ms(local_ms: float, world: int, device) -> float:
@@ -317,6 +330,7 @@ def main():
     flush = work_bytes < (256 << 20)
     scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
     barrier()
+    t_wall0 = time.time()
     for i in range(args.steps):
         if flush:
             scrub.fill_(i & 0xFF)
@@ -324,6 +338,7 @@ def main():
         step(dq, dk, dv, out)
         ends[i].record(stream)
     barrier()
+    sampler.mark(t_wall0, time.time())
     clocks = sampler.stop() if rank == 0 else None
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(kernel_ms) if flush else starts[0].elapsed_time(ends[-1])

@@ -453,12 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ad = qt + (off - C::kChunks128K * 128) / 16;
             bd = kt + (off - C::kChunks128K * 128) / 16;
           }
-          if (leader) {
-            if constexpr (FP8) mma_f8_ss(tmem + C::kColS, ad, bd, idesc_s, ks > 0);
-            else mma_f16_ss(tmem + C::kColS, ad, bd, idesc_s, ks > 0);
-          }
+          if constexpr (FP8) mma_f8_ss(tmem + C::kColS, ad, bd, idesc_s, ks > 0);
+          else mma_f16_ss(tmem + C::kColS, ad, bd, idesc_s, ks > 0);
         }
-        if (leader) tc_commit(smem_u32(&ctl.s_full[t]));
+        tc_commit(smem_u32(&ctl.s_full[t]));
       };
       // O_t (| l_t) += P_t x [V | 1]
       auto issue_pv = [&](int t, uint32_t st, bool first) {
@@ -470,14 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < C::kPVSteps; ++ks) {
           const uint64_t vdk = vd + (ks * C::kKeysPerStep * C::kVAtomRow) / 16;
           const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
-          if (leader) {
-            if constexpr (FP8) {
-              // K step ks covers keys [32ks, 32ks+32): its e8m0 scale is byte ks of the scale word
-              mma_mxf8_ts(o, pa + ks * 8, vdk, idesc_block_scaled(kFmtE4M3, kFmtE4M3, true, kBlockM, C::kNO, ks, 0),
-                          tmem + C::col_sfa(t), tmem + C::kColSFB, acc);
-            } else {
-              mma_f16_ts(o, pa + ks * 8, vdk, idesc_dense(kFmtBF16, kFmtBF16, false, true, kBlockM, C::kNO), acc);
-            }
+          if constexpr (FP8) {
+            // K step ks covers keys [32ks, 32ks+32): its e8m0 scale is byte ks of the scale word
+            mma_mxf8_ts(o, pa + ks * 8, vdk, idesc_block_scaled(kFmtE4M3, kFmtE4M3, true, kBlockM, C::kNO, ks, 0),
+                           tmem + C::col_sfa(t), tmem + C::kColSFB, acc);
+          } else {
+            mma_f16_ts(o, pa + ks * 8, vdk, idesc_dense(kFmtBF16, kFmtBF16, false, true, kBlockM, C::kNO), acc);
           }
         }
       };
@@ -487,11 +483,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n0 = tiles_for<BN>(p, u.r0, 0), n1 = tiles_for<BN>(p, u.r0, 1);
         const int nkv = n1 > n0 ? n1 : n0;
         if (n0 > 0) {
-          ok = mbar_wait(smem_u32(&ctl.q_full[0]), q_cnt[0] & 1, abort_flag, kWaitLimit);
+          ok = mbar_wait_warp(smem_u32(&ctl.q_full[0]), q_cnt[0] & 1, abort_flag, kWaitLimit);
           ++q_cnt[0];
         }
         if (ok && n1 > 0) {
-          ok = mbar_wait(smem_u32(&ctl.q_full[1]), q_cnt[1] & 1, abort_flag, kWaitLimit);
+          ok = mbar_wait_warp(smem_u32(&ctl.q_full[1]), q_cnt[1] & 1, abort_flag, kWaitLimit);
           ++q_cnt[1];
         }
         if (!ok) break;
@@ -501,14 +497,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto do_pv = [&](int t, int j) -> bool {
           const uint32_t st = (kv_cnt + j) % C::kStages;
           if constexpr (C::kSplitKV) {
-            if (!mbar_wait(smem_u32(&ctl.v_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag, kWaitLimit))
+            if (!mbar_wait_warp(smem_u32(&ctl.v_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag, kWaitLimit))
               return false;
             tc_fence_after();
           }
           issue_pv(t, st, j == 0);
-          if (leader) tc_commit(smem_u32(&ctl.pv_done[t]));
+          tc_commit(smem_u32(&ctl.pv_done[t]));
           const bool pv0_last = n1 == 0 || (j == n0 - 1 && n1 > n0);
-          if (leader && (t == 0) == pv0_last)
+          if ((t == 0) == pv0_last)
             tc_commit(smem_u32(C::kSplitKV ? &ctl.v_empty[st] : &ctl.k_empty[st]));
           return true;
         };
@@ -519,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto wait_read = [&]() -> bool {
           rj = -1;
           if (!read_pending) return true;
-          if (!mbar_wait(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit)) return false;
+          if (!mbar_wait_warp(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit)) return false;
           read_pending = false;
           tc_fence_after();
           if (last_j >= 1) {
@@ -537,40 +533,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j >= 1 && j < n0 && n1 > 0) {
             // steady state (both query tiles active): S0(j), PV1(j-2), S1(j), PV0(j-1)
             const uint32_t st = (kv_cnt + j) % C::kStages;
-            if (!(ok = mbar_wait(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit))) break;
-            if (!(ok = mbar_wait(smem_u32(&ctl.k_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag,
+            if (!(ok = mbar_wait_warp(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit))) break;
+            if (!(ok = mbar_wait_warp(smem_u32(&ctl.k_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag,
                                  kWaitLimit)))
               break;
             tc_fence_after();
             issue_s(0, st);
-            if (leader && j == n0 - 1) tc_commit(smem_u32(&ctl.q_empty[0]));
+            if (j == n0 - 1) tc_commit(smem_u32(&ctl.q_empty[0]));
             if (j >= 2) {
               const uint32_t st2 = (kv_cnt + j - 2) % C::kStages;
               if constexpr (C::kSplitKV) {
-                if (!(ok = mbar_wait(smem_u32(&ctl.v_full[st2]), ((kv_cnt + j - 2) / C::kStages) & 1, abort_flag,
+                if (!(ok = mbar_wait_warp(smem_u32(&ctl.v_full[st2]), ((kv_cnt + j - 2) / C::kStages) & 1, abort_flag,
                                      kWaitLimit)))
                   break;
                 tc_fence_after();
               }
               issue_pv(1, st2, j == 2);
-              if (leader) {
-                tc_commit(smem_u32(&ctl.pv_done[1]));
-                tc_commit(smem_u32(C::kSplitKV ? &ctl.v_empty[st2] : &ctl.k_empty[st2]));
-              }
+              tc_commit(smem_u32(&ctl.pv_done[1]));
+              tc_commit(smem_u32(C::kSplitKV ? &ctl.v_empty[st2] : &ctl.k_empty[st2]));
             }
-            if (!(ok = mbar_wait(smem_u32(&ctl.s_free), s_seq & 1, abort_flag, kWaitLimit))) break;
+            if (!(ok = mbar_wait_warp(smem_u32(&ctl.s_free), s_seq & 1, abort_flag, kWaitLimit))) break;
             tc_fence_after();
             issue_s(1, st);
-            if (C::kSplitKV && leader) tc_commit(smem_u32(&ctl.k_empty[st]));  // S1(j): last reader of K tile j
+            if (C::kSplitKV) tc_commit(smem_u32(&ctl.k_empty[st]));  // S1(j): last reader of K tile j
             const uint32_t st1 = (kv_cnt + j - 1) % C::kStages;
             if constexpr (C::kSplitKV) {
-              if (!(ok = mbar_wait(smem_u32(&ctl.v_full[st1]), ((kv_cnt + j - 1) / C::kStages) & 1, abort_flag,
+              if (!(ok = mbar_wait_warp(smem_u32(&ctl.v_full[st1]), ((kv_cnt + j - 1) / C::kStages) & 1, abort_flag,
                                    kWaitLimit)))
                 break;
               tc_fence_after();
             }
             issue_pv(0, st1, j == 1);
-            if (leader) tc_commit(smem_u32(&ctl.pv_done[0]));
+            tc_commit(smem_u32(&ctl.pv_done[0]));
             s_seq += 2;
             last_t = 1;
             last_j = j;
@@ -585,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool pv_first = rj >= 0 && rt == t;
             if (pv_first && !(ok = do_pv(rt, rj))) break;
             if (t == 0 || j >= n0) {  // first score tile of K tile j
-              if (!(ok = mbar_wait(smem_u32(&ctl.k_full[(kv_cnt + j) % C::kStages]),
+              if (!(ok = mbar_wait_warp(smem_u32(&ctl.k_full[(kv_cnt + j) % C::kStages]),
                                    ((kv_cnt + j) / C::kStages) & 1, abort_flag, kWaitLimit)))
                 break;
               tc_fence_after();
@@ -595,9 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             read_pending = true;
             last_t = t;
             last_j = j;
-            if (leader && j == (t ? n1 : n0) - 1) tc_commit(smem_u32(&ctl.q_empty[t]));
+            if (j == (t ? n1 : n0) - 1) tc_commit(smem_u32(&ctl.q_empty[t]));
             // the last score MMA reading K tile j: S1(j), or S0(j) when query tile 1 has no tile j
-            if (C::kSplitKV && leader && (t == 1 || j >= n1))
+            if (C::kSplitKV && (t == 1 || j >= n1))
               tc_commit(smem_u32(&ctl.k_empty[(kv_cnt + j) % C::kStages]));
             if (rj >= 0 && !pv_first && !(ok = do_pv(rt, rj))) break;
           }
@@ -611,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
           const int nt = t ? n1 : n0;
           if (nt == 0) continue;
-          if (!(ok = mbar_wait(smem_u32(&ctl.p_full[t]), p_cnt[t] & 1, abort_flag, kWaitLimit))) break;
+          if (!(ok = mbar_wait_warp(smem_u32(&ctl.p_full[t]), p_cnt[t] & 1, abort_flag, kWaitLimit))) break;
           ++p_cnt[t];
           tc_fence_after();
           if (!(ok = do_pv(t, nt - 1))) break;
@@ -621,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && leader) give_up();
       // drain: all MMAs issued by this warp complete before TMEM is released
       const int never = 0;
-      if (leader) tc_commit(smem_u32(&ctl.drain));
-      mbar_wait(smem_u32(&ctl.drain), 0, &never, kWaitLimit);
+      tc_commit(smem_u32(&ctl.drain));
+      mbar_wait_warp(smem_u32(&ctl.drain), 0, &never, kWaitLimit);
     }
   } else if (warp == 2) {
     // =========================== TMA producer: V (short rings) ===========================
