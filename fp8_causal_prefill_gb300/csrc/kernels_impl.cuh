@@ -10,6 +10,11 @@ int smem_bytes() {
   return Cfg<FP8, DQK, DV, tile_keys<FP8, DQK, DV>()>::kSmemBytes;
 }
 
+template <bool FP8, int DQK, int DV>
+int epi_cols() {
+  return Cfg<FP8, DQK, DV, tile_keys<FP8, DQK, DV>()>::kEpiCols;
+}
+
 template <bool FP8, int DQK, int DV, bool EXACT>
 cudaError_t launch_fwd(const LaunchArgs& a) {
   constexpr int BN = tile_keys<FP8, DQK, DV>();

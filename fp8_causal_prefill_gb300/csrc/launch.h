@@ -8,6 +8,7 @@ namespace zyfa {
 // 4-D tensor maps over [B][S][heads][D]; *0 move 128-byte chunks of a row, *1 its 64-byte tail chunk.
 struct Maps {
   CUtensorMap q0, q1, k0, k1, v;
+  CUtensorMap o;  // bf16 output, stored by TMA from a per-warp staging tile
 };
 
 struct LaunchArgs {
@@ -42,5 +43,10 @@ cudaError_t launch_fwd(const LaunchArgs& a);
 // Dynamic shared memory the kernel instantiation needs (bytes).
 template <bool FP8, int DQK, int DV>
 int smem_bytes();
+
+// Output columns per TMA store box of the instantiation's epilogue (32, or 16 where shared memory
+// is short); the output map's box is 32 rows x this many columns.
+template <bool FP8, int DQK, int DV>
+int epi_cols();
 
 }  // namespace zyfa

@@ -129,6 +129,10 @@ zyfa_status_t run(zyfa::LaunchArgs& a, const void* q, const void* k, const void*
   // V: MN-major tiles, one swizzle atom per 128 bytes (or the whole 64-byte row) of the value row
   ok &= make_map(&m.v, v, FP8, DV, a.H_kv, a.S, a.B, kRowV >= 128 ? kChunk : DV, BN,
                  kRowV >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+  // output: per-warp boxes of 32 rows x kEpiCols bf16 columns, swizzled like the staging tile
+  const int epi_cols = zyfa::epi_cols<FP8, DQK, DV>();
+  ok &= make_map(&m.o, a.out, false, DV, a.H, a.S, a.B, epi_cols, 32,
+                 epi_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
   if (!ok) return ZYFA_ERR_CUDA;
   // maps the instantiation never touches are copies of valid ones
   if (kRowK < 128) { m.q0 = m.q1; m.k0 = m.k1; }

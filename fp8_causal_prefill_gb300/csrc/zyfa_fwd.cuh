@@ -102,7 +102,14 @@ struct Cfg {
   static constexpr int kStagesRaw = (kSmemBudget - kFixedBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static_assert(kStages >= 2, "not enough shared memory for two K/V stages");
-  static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
+  // epilogue: each softmax warp stages 32 rows x kEpiCols bf16 of its output (64- or 32-byte rows,
+  // swizzled) for a TMA store; 64-byte rows where the shared memory allows
+  static constexpr int kSmemMax = 232448;  // opt-in limit per block on sm_103
+  static constexpr int kEpiCols = kFixedBytes + kStages * kStageBytes + 8 * 2048 <= kSmemMax ? 32 : 16;
+  static constexpr int kEpiWarpBytes = 32 * kEpiCols * 2;
+  static_assert(DV % kEpiCols == 0, "whole epilogue boxes");
+  static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes + 8 * kEpiWarpBytes;
+  static_assert(kSmemBytes <= kSmemMax, "shared memory");
   // tensor memory columns
   static constexpr uint32_t kColS = 0;
   __device__ static constexpr uint32_t col_o(int t) { return 128u + static_cast<uint32_t>(kNO) * t; }
@@ -296,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // ---- shared memory: [Q0 | Q1 | stage 0 (K|V) | ... | ones atom], 1024-byte aligned ----
+  // ---- shared memory: [Q0 | Q1 | K/V slots | ones atom | epilogue tiles], 1024-byte aligned ----
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw_addr);
@@ -306,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // leading-dimension offset (a positive distance from each stage)
   // split rings: all K slots, then all V slots; one ring: each slot holds a K tile and its V tile
   const uint32_t s_ones = s_stages + C::kStages * C::kStageBytes;
+  const uint32_t s_epi = s_ones + C::kOnesBytes;  // 8 softmax warps x kEpiWarpBytes
   auto k_stage = [&](int s) { return s_stages + s * (C::kSplitKV ? C::kKStageBytes : C::kStageBytes); };
   auto v_stage = [&](int s) {
     return C::kSplitKV ? s_stages + C::kStages * C::kKStageBytes + s * C::kVStageBytes
@@ -664,6 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_addr + C::kColS;
     const uint32_t tO = tmem + lane_addr + C::col_o(t);
     const uint32_t tP = tmem + lane_addr + C::col_p(t);
+    const uint32_t epi_tile = s_epi + (warp - 4) * C::kEpiWarpBytes;  // 1024-byte aligned
 
     // score scale a (FP8: 1/8-binade units, with the descales; BF16: binades) and output scale dv,
     // per unit when the descales are per (batch, KV head)
@@ -818,27 +827,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse[(static_cast<size_t>(u.b) * p.H + u.h) * p.S + row] =
             (static_cast<float>(m_ref) + __log2f(l)) * 0.6931471805599453f;
       }
-      __nv_bfloat16* orow = p.out + ((static_cast<size_t>(u.b) * p.S + (row_ok ? row : 0)) * p.H + u.h) * DV;
+      // The warp's 32 rows go out through its staging tile, kEpiCols columns at a time, as TMA
+      // stores (each row is contiguous in global memory only within itself, so stores straight from
+      // the row-per-lane registers would touch 32 lines per instruction); rows past S are clipped.
+      constexpr int kCW = C::kEpiCols, kPieces = kCW * 2 / 16;  // 16-byte pieces per staged row
 #pragma unroll
-      for (int c = 0; c < DV / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tO + 32 * c, r);
+      for (int c = 0; c < DV / kCW; ++c) {
+        uint32_t r[kCW];
+        if constexpr (kCW == 32) tmem_ld32(tO + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r));
+        else tmem_ld16(tO + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(r));
         tmem_wait_ld();
         tmem_ld_fence(r);
-        uint32_t packed[16];
+        uint32_t packed[kCW / 2];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < kCW / 2; ++i)
           packed[i] = cvt_bf16x2(__uint_as_float(r[2 * i + 1]) * inv, __uint_as_float(r[2 * i]) * inv);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+        // the previous store from this tile has finished reading it
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        // row `lane` at lane * kCW * 2 bytes; 16-byte piece i at (i ^ swz), the TMA swizzle of the
+        // map (64-byte rows: piece ^= (row >> 1) & 3; 32-byte rows: piece ^= (row >> 2) & 1)
+        const int swz = kPieces == 4 ? (lane >> 1) & 3 : (lane >> 2) & 1;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        for (int i = 0; i < kPieces; ++i)
+          st_shared_v4(epi_tile + lane * (kCW * 2) + ((i ^ swz) << 4), packed[4 * i], packed[4 * i + 1],
+                       packed[4 * i + 2], packed[4 * i + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_4d(&maps.o, epi_tile, c * kCW, u.h, row0 + quarter * 32, u.b);
+          bulk_commit();
         }
       }
       tc_fence_before();
     }
     if (!ok && lane == 0) give_up();
+    if (lane == 0) bulk_wait_all();  // the output stores are complete before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
