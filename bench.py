@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--p-mode", choices=["lean", "exact"], default="lean",
                     help="FP8 probabilities: Lean P (the method) or exact exponential (the ablation)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--host-chunks", type=int, default=0,
+                    help="chunks of the host-buffer call in the e2e leg (0 = the library default, 4)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
     return ap.parse_args()
@@ -427,7 +429,7 @@ def main():
                                                hout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                                out.data_ptr(), sh.B, sh.S, sh.H, sh.H_kv, sh.D_qk, sh.D_v, 0.0,
                                                dtype_code, dptr, dptr + 4 if dptr else 0, dptr + 8 if dptr else 0,
-                                               0, sptr)
+                                               args.host_chunks, sptr)
             if st != 0:
                 raise api.ZyfaError(st, "zyfa_attn_fwd_causal_host")
         for _ in range(2):
@@ -442,7 +444,8 @@ def main():
         te = slowest_rank_ms(e0.elapsed_time(e1) / n_e2e, world, dev)
         e2e = {"value": job_throughput(flops, world, te), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": te,
-               "steps": n_e2e, "call": "zyfa_attn_fwd_causal_host (pinned host buffers, 4 chunks)"}
+               "steps": n_e2e, "call": "zyfa_attn_fwd_causal_host (pinned host buffers)",
+               "chunks": args.host_chunks or 4}
 
     if rank == 0:
         peaks, src = load_peaks()
