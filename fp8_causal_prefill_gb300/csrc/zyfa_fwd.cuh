@@ -541,10 +541,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j >= 1 && j < n0 && n1 > 0) {
             // steady state (both query tiles active): S0(j), PV1(j-2), S1(j), PV0(j-1)
             const uint32_t st = (kv_cnt + j) % C::kStages;
-            if (!(ok = mbar_wait_warp(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit))) break;
+            // K first: it is normally in place long before the read, so checking it while the read is
+            // outstanding keeps the check off the path from the read to the next score MMA
             if (!(ok = mbar_wait_warp(smem_u32(&ctl.k_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag,
                                  kWaitLimit)))
               break;
+            if (!(ok = mbar_wait_warp(smem_u32(&ctl.s_free), (s_seq - 1) & 1, abort_flag, kWaitLimit))) break;
             tc_fence_after();
             issue_s(0, st);
             if (j == n0 - 1) tc_commit(smem_u32(&ctl.q_empty[0]));
@@ -582,16 +584,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (j >= (t ? n1 : n0)) continue;
-            if (!(ok = wait_read())) break;
-            // a PV of the same query tile goes before its next score MMA, one of the other tile after it
-            const bool pv_first = rj >= 0 && rt == t;
-            if (pv_first && !(ok = do_pv(rt, rj))) break;
             if (t == 0 || j >= n0) {  // first score tile of K tile j
               if (!(ok = mbar_wait_warp(smem_u32(&ctl.k_full[(kv_cnt + j) % C::kStages]),
                                    ((kv_cnt + j) / C::kStages) & 1, abort_flag, kWaitLimit)))
                 break;
               tc_fence_after();
             }
+            if (!(ok = wait_read())) break;
+            // a PV of the same query tile goes before its next score MMA, one of the other tile after it
+            const bool pv_first = rj >= 0 && rt == t;
+            if (pv_first && !(ok = do_pv(rt, rj))) break;
             issue_s(t, (kv_cnt + j) % C::kStages);
             ++s_seq;
             read_pending = true;
