@@ -108,7 +108,10 @@ struct Cfg {
   static constexpr int kEpiCols = kFixedBytes + kStages * kStageBytes + 8 * 2048 <= kSmemMax ? 32 : 16;
   static constexpr int kEpiWarpBytes = 32 * kEpiCols * 2;
   static_assert(DV % kEpiCols == 0, "whole epilogue boxes");
-  static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes + 8 * kEpiWarpBytes;
+  // two tiles per warp where they fit: a box is staged while the previous one is still being stored
+  static constexpr int kEpiBufs =
+      kFixedBytes + kStages * kStageBytes + 2 * 8 * kEpiWarpBytes <= kSmemMax ? 2 : 1;
+  static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes + kEpiBufs * 8 * kEpiWarpBytes;
   static_assert(kSmemBytes <= kSmemMax, "shared memory");
   // tensor memory columns
   static constexpr uint32_t kColS = 0;
@@ -232,18 +235,35 @@ __device__ __forceinline__ float exp2i(int d) {
   return d < -126 ? 0.0f : __int_as_float((127 + d) << 23);
 }
 
+// Two fp32 lanes in one 64-bit register, for the packed multiply-add.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t cvt_relu_f16x2_pair(uint64_t t) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(t));
+  return cvt_relu_f16x2(hi, lo);
+}
+
 // Lean-P codes of the 64 scores of one scale block with exponent e: t = fma(s, a, 55.625 - 8e) scaled
-// by 2^-24, so the f16 subnormal that the rounding conversion produces carries the integer code in
-// its low byte (negative values clamp to 0).  Four codes per 32-bit word, key order = byte order.
+// by 2^-24 (two scores per packed fp32 multiply-add, each lane rounded as a scalar fma), so the f16
+// subnormal that the rounding conversion produces carries the integer code in its low byte
+// (negative values clamp to 0).  Four codes per 32-bit word, key order = byte order.
 __device__ __forceinline__ void leanp_block(const float* s, float a24, int e, uint32_t (&pw)[16]) {
   const float c24 = __fmul_rn(kLeanPC0 - 8.0f * static_cast<float>(e), 0x1p-24f);
+  const uint64_t a2 = pack2(a24, a24), c2 = pack2(c24, c24);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float t0 = __fmaf_rn(s[4 * i + 0], a24, c24);
-    const float t1 = __fmaf_rn(s[4 * i + 1], a24, c24);
-    const float t2 = __fmaf_rn(s[4 * i + 2], a24, c24);
-    const float t3 = __fmaf_rn(s[4 * i + 3], a24, c24);
-    pw[i] = prmt(cvt_relu_f16x2(t1, t0), cvt_relu_f16x2(t3, t2), 0x6420u);
+    const uint64_t t01 = ffma2(pack2(s[4 * i + 0], s[4 * i + 1]), a2, c2);
+    const uint64_t t23 = ffma2(pack2(s[4 * i + 2], s[4 * i + 3]), a2, c2);
+    pw[i] = prmt(cvt_relu_f16x2_pair(t01), cvt_relu_f16x2_pair(t23), 0x6420u);
   }
 }
 
@@ -674,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_addr + C::kColS;
     const uint32_t tO = tmem + lane_addr + C::col_o(t);
     const uint32_t tP = tmem + lane_addr + C::col_p(t);
-    const uint32_t epi_tile = s_epi + (warp - 4) * C::kEpiWarpBytes;  // 1024-byte aligned
+    const uint32_t epi_tile = s_epi + (warp - 4) * C::kEpiBufs * C::kEpiWarpBytes;  // 1024-byte aligned
 
     // score scale a (FP8: 1/8-binade units, with the descales; BF16: binades) and output scale dv,
     // per unit when the descales are per (batch, KV head)
@@ -813,6 +833,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++pv_ph;
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
+      // all of O (and the FP8 row sum) in one round trip
+      uint32_t o[DV];
+#pragma unroll
+      for (int c = 0; c < DV / 32; ++c) tmem_ld32(tO + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(o + 32 * c));
       float l;
       if constexpr (FP8) {
         uint32_t lv[1];
@@ -821,8 +845,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_fence(lv);
         l = __uint_as_float(lv[0]);
       } else {
+        tmem_wait_ld();
         l = l_bf16;
       }
+      tmem_ld_fence(o);
       const float inv = __fdiv_rn(out_scale, l);
       if (p.lse != nullptr && row_ok) {
         // ln sum_j exp(s_ij) = (M + log2 l) ln 2: l sums the rounded weights relative to 2^M
@@ -835,29 +861,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kCW = C::kEpiCols, kPieces = kCW * 2 / 16;  // 16-byte pieces per staged row
 #pragma unroll
       for (int c = 0; c < DV / kCW; ++c) {
-        uint32_t r[kCW];
-        if constexpr (kCW == 32) tmem_ld32(tO + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r));
-        else tmem_ld16(tO + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(r));
-        tmem_wait_ld();
-        tmem_ld_fence(r);
+        const uint32_t* r = o + c * kCW;
         uint32_t packed[kCW / 2];
 #pragma unroll
         for (int i = 0; i < kCW / 2; ++i)
           packed[i] = cvt_bf16x2(__uint_as_float(r[2 * i + 1]) * inv, __uint_as_float(r[2 * i]) * inv);
-        // the previous store from this tile has finished reading it
-        if (lane == 0) bulk_wait_read_all();
+        // the store that last used this tile has finished reading it
+        const uint32_t tile = epi_tile + (c % C::kEpiBufs) * C::kEpiWarpBytes;
+        if (lane == 0) {
+          if constexpr (C::kEpiBufs == 2) bulk_wait_read_but1();
+          else bulk_wait_read_all();
+        }
         __syncwarp();
         // row `lane` at lane * kCW * 2 bytes; 16-byte piece i at (i ^ swz), the TMA swizzle of the
         // map (64-byte rows: piece ^= (row >> 1) & 3; 32-byte rows: piece ^= (row >> 2) & 1)
         const int swz = kPieces == 4 ? (lane >> 1) & 3 : (lane >> 2) & 1;
 #pragma unroll
         for (int i = 0; i < kPieces; ++i)
-          st_shared_v4(epi_tile + lane * (kCW * 2) + ((i ^ swz) << 4), packed[4 * i], packed[4 * i + 1],
+          st_shared_v4(tile + lane * (kCW * 2) + ((i ^ swz) << 4), packed[4 * i], packed[4 * i + 1],
                        packed[4 * i + 2], packed[4 * i + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_4d(&maps.o, epi_tile, c * kCW, u.h, row0 + quarter * 32, u.b);
+          tma_store_4d(&maps.o, tile, c * kCW, u.h, row0 + quarter * 32, u.b);
           bulk_commit();
         }
       }
