@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--dtype", choices=["fp8", "bf16"], default="fp8")
     ap.add_argument("--config", default="bench32k")
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling a smaller case)")
+    ap.add_argument("--seq", type=int, default=0, help="override S (a sequence-length sweep)")
     ap.add_argument("--energy", action="store_true",
                     help="also measure energy per step (NVML total-energy counter over a >= 2 s loop)")
     ap.add_argument("--hadamard", action="store_true",
@@ -80,6 +81,8 @@ def shape_for(args):
     if args.heads:
         hkv = max(1, args.heads * sh.H_kv // sh.H)
         sh = Shape(sh.B, sh.S, args.heads, hkv, sh.D_qk, sh.D_v, sh.kind)
+    if args.seq:
+        sh = Shape(sh.B, args.seq, sh.H, sh.H_kv, sh.D_qk, sh.D_v, sh.kind)
     return sh
 
 
@@ -461,15 +464,15 @@ def main():
             with open(tpath) as f:
                 td = json.load(f)
             key = f"{args.dtype}:{args.config}" + (":exact" if args.p_mode == "exact" else "")
-            if key in td and not args.heads and td[key].get("kernel_sha256") == kernel_source_hash():
+            if key in td and not args.heads and not args.seq and td[key].get("kernel_sha256") == kernel_source_hash():
                 traffic = td[key].get("bytes_per_launch")
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3" if is_fp8 else "bf16", "data": "synthetic",
             "config": {"workload": workload_name(sh, args.dtype, args.p_mode),
-                       "l2": (f"working set {work_bytes / 1e6:.0f} MB fits the 129 MB L2: flushed between steps "
-                              f"(256 MB write outside the timed events; value from per-step events)" if flush else
+                       "l2": (f"working set {work_bytes / 1e6:.0f} MB is under twice the 129 MB L2: flushed between "
+                              f"steps (256 MB write outside the timed events; value from per-step events)" if flush else
                               f"working set {work_bytes / 1e6:.0f} MB (inputs + output) exceeds the 129 MB L2; "
                               f"no flush"),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
