@@ -506,6 +506,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
 
+      // PV_t(j) of a unit whose K/V tiles start at ring position kvb and whose query tiles have n0_ /
+      // n1_ K/V tiles, announced on pv_done.  A K/V stage is released after the later of its (at most
+      // two) PVs.
+      auto do_pv_at = [&](int t, int j, uint32_t kvb, int n0_, int n1_) -> bool {
+        const uint32_t st = (kvb + j) % C::kStages;
+        if constexpr (C::kSplitKV) {
+          if (!mbar_wait_warp(smem_u32(&ctl.v_full[st]), ((kvb + j) / C::kStages) & 1, abort_flag, kWaitLimit))
+            return false;
+          tc_fence_after();
+        }
+        issue_pv(t, st, j == 0);
+        tc_commit(smem_u32(&ctl.pv_done[t]));
+        const bool pv0_last = n1_ == 0 || (j == n0_ - 1 && n1_ > n0_);
+        if ((t == 0) == pv0_last)
+          tc_commit(smem_u32(C::kSplitKV ? &ctl.v_empty[st] : &ctl.k_empty[st]));
+        return true;
+      };
+      // The last PV of each query tile waits for that tile's final P (p_full).  It is issued after
+      // the next unit's first score MMA, so that score tile is not held behind the slower warpgroup's
+      // last softmax; per tile the PVs stay in order.
+      // the pending last PVs all belong to one unit: its K/V ring base and tile counts
+      int tail_n[2] = {0, 0};
+      uint32_t tail_kvb = 0;
+      auto issue_tails = [&]() -> bool {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (tail_n[t] == 0) continue;
+          if (!mbar_wait_warp(smem_u32(&ctl.p_full[t]), p_cnt[t] & 1, abort_flag, kWaitLimit)) return false;
+          ++p_cnt[t];
+          tc_fence_after();
+          if (!do_pv_at(t, tail_n[t] - 1, tail_kvb, tail_n[0], tail_n[1])) return false;
+        }
+        tail_n[0] = tail_n[1] = 0;
+        return true;
+      };
+
       Unit u;
       for (int round = 0; ok && unit_at(p, round, u); ++round) {
         const int n0 = tiles_for<BN>(p, u.r0, 0), n1 = tiles_for<BN>(p, u.r0, 1);
@@ -520,22 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
 
-        // PV_t(j), announced on pv_done.  A K/V stage is released after the later of its (at most
-        // two) PVs.
-        auto do_pv = [&](int t, int j) -> bool {
-          const uint32_t st = (kv_cnt + j) % C::kStages;
-          if constexpr (C::kSplitKV) {
-            if (!mbar_wait_warp(smem_u32(&ctl.v_full[st]), ((kv_cnt + j) / C::kStages) & 1, abort_flag, kWaitLimit))
-              return false;
-            tc_fence_after();
-          }
-          issue_pv(t, st, j == 0);
-          tc_commit(smem_u32(&ctl.pv_done[t]));
-          const bool pv0_last = n1 == 0 || (j == n0 - 1 && n1 > n0);
-          if ((t == 0) == pv0_last)
-            tc_commit(smem_u32(C::kSplitKV ? &ctl.v_empty[st] : &ctl.k_empty[st]));
-          return true;
-        };
+        auto do_pv = [&](int t, int j) -> bool { return do_pv_at(t, j, kv_cnt, n0, n1); };
         // Waits until the last score tile issued has been copied out of the shared S buffer.  Its
         // reader stored P of its previous tile before that, so the PV of that tile may follow; that
         // tile is returned in rt / rj (rj < 0: nothing to unlock).
@@ -624,24 +645,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (C::kSplitKV && (t == 1 || j >= n1))
               tc_commit(smem_u32(&ctl.k_empty[(kv_cnt + j) % C::kStages]));
             if (rj >= 0 && !pv_first && !(ok = do_pv(rt, rj))) break;
+            if (t == 0 && j == 0 && !(ok = issue_tails())) break;
           }
         }
         if (!ok) break;
         // unit end: the read of the last score tile unlocks one more PV; the last PV of each query
-        // tile waits for the softmax warpgroup's P directly
+        // tile (which waits for its final P) goes with the next unit's first score MMA
         if (!(ok = wait_read())) break;
         if (rj >= 0 && !(ok = do_pv(rt, rj))) break;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int nt = t ? n1 : n0;
-          if (nt == 0) continue;
-          if (!(ok = mbar_wait_warp(smem_u32(&ctl.p_full[t]), p_cnt[t] & 1, abort_flag, kWaitLimit))) break;
-          ++p_cnt[t];
-          tc_fence_after();
-          if (!(ok = do_pv(t, nt - 1))) break;
-        }
+        tail_n[0] = n0;
+        tail_n[1] = n1;
+        tail_kvb = kv_cnt;
         kv_cnt += nkv;
       }
+      if (ok) ok = issue_tails();
       if (!ok && leader) give_up();
       // drain: all MMAs issued by this warp complete before TMEM is released
       const int never = 0;
