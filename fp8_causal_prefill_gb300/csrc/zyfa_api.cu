@@ -291,13 +291,15 @@ zyfa_status_t zyfa_attn_fwd_causal_host(const void* q_host, const void* k_host, 
     ok = copy_rows(q_dev, q_host, row_q, r0, r1, cudaMemcpyHostToDevice, up) &&
          copy_rows(k_dev, k_host, row_k, r0, r1, cudaMemcpyHostToDevice, up) &&
          copy_rows(v_dev, v_host, row_v, r0, r1, cudaMemcpyHostToDevice, up) &&
-         cudaEventRecord(ev.e[1 + 2 * c], up) == cudaSuccess && cudaStreamWaitEvent(stream, ev.e[1 + 2 * c], 0) == cudaSuccess;
+         cudaEventRecord(ev.e[1 + 2 * c], up) == cudaSuccess &&
+         cudaStreamWaitEvent(stream, ev.e[1 + 2 * c], 0) == cudaSuccess;
     if (!ok) break;
     // query blocks [qb0, qb1) read keys [0, r1): every one of them arrived with this or an earlier chunk
     st = attn_fwd(q_dev, k_dev, v_dev, out_dev, B, S, H, H_kv, D_qk, D_v, softmax_scale, dtype, q_descale, k_descale,
                   v_descale, nullptr, stream, 0, qb0, qb1);
     if (st != ZYFA_OK) break;
-    ok = cudaEventRecord(ev.e[2 + 2 * c], stream) == cudaSuccess && cudaStreamWaitEvent(down, ev.e[2 + 2 * c], 0) == cudaSuccess &&
+    ok = cudaEventRecord(ev.e[2 + 2 * c], stream) == cudaSuccess &&
+         cudaStreamWaitEvent(down, ev.e[2 + 2 * c], 0) == cudaSuccess &&
          copy_rows(out_host, out_dev, row_o, r0, r1, cudaMemcpyDeviceToHost, down);
   }
   // the caller's stream resumes once the last output rows are back on the host

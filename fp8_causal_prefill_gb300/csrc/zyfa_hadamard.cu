@@ -4,8 +4,9 @@
 //
 // x [rows][D] bf16 -> y = x R with R block-diagonal, normalised Walsh-Hadamard blocks of n = 128
 // (D = 128) or 64 (D = 64, 192); the usual FP8 scale pair scale = fl32(448 / max|y|),
-// descale = fl32(max|y| / 448) (both 1 if the maximum is 0); codes = rne_e4m3_satfinite(fl32(y * scale)).  y is computed in fp32 by the radix-2 transform,
-// stages h = 1, 2, 4, ... with the butterflies (a + b, a - b), then one multiply by fl32(1/sqrt(n)).
+// descale = fl32(max|y| / 448) (both 1 if the maximum is 0); codes =
+// rne_e4m3_satfinite(fl32(y * scale)).  y is computed in fp32 by the radix-2 transform, stages
+// h = 1, 2, 4, ... with the butterflies (a + b, a - b), then one multiply by fl32(1/sqrt(n)).
 //
 // The per-tensor maximum needs a pass over the whole tensor before any code can be written, so the
 // work is two launches over the same rows: pass 1 rotates and writes one partial maximum per block of
