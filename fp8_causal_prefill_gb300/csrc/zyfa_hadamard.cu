@@ -15,7 +15,9 @@
 // fixed array inside this library (zyfa_hadamard_quantize_e4m3_noalloc).
 //
 // HBM-bound: per element 2 bytes read twice and 1 byte written.  Each thread rotates whole Hadamard
-// blocks of one row in registers (no cross-lane traffic); a CTA of 128 threads covers 128 rows.
+// blocks of one row in registers (no cross-lane traffic); a CTA of 128 threads covers 128 rows.  A
+// thread's next row is copied into shared memory (cp.async, a padded slot per thread) while it
+// rotates the current one, which keeps the loads of the next rows in flight behind the arithmetic.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -36,18 +38,45 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   return r;
 }
 
+// Packed fp32 pairs: each lane rounded as its scalar operation.
+__device__ __forceinline__ uint64_t pk(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // One N-wide Hadamard block held by one thread, transformed in place: stages h = 1, 2, 4, ...,
-// butterflies (a + b, a - b), then one multiply by fl32(1/sqrt(N)).
+// butterflies (a + b, a - b), then one multiply by fl32(1/sqrt(N)).  From h = 2 on, the butterflies
+// of neighbouring elements go through packed pairs.
 template <int N>
 __device__ __forceinline__ void fwht(float (&v)[N]) {
 #pragma unroll
-  for (int h = 1; h < N; h *= 2) {
+  for (int i = 0; i < N; i += 2) {
+    const float a = v[i], b = v[i + 1];
+    v[i] = __fadd_rn(a, b);
+    v[i + 1] = __fsub_rn(a, b);
+  }
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
+  for (int h = 2; h < N; h *= 2) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
       if ((i & h) == 0) {
-        const float a = v[i], b = v[i + h];
-        v[i] = __fadd_rn(a, b);
-        v[i + h] = __fsub_rn(a, b);
+        const uint64_t a = pk(v[i], v[i + 1]), b = pk(v[i + h], v[i + h + 1]);
+        upk(add2(a, b), v[i], v[i + 1]);
+        upk(sub2(a, b), v[i + h], v[i + h + 1]);
       }
     }
   }
@@ -56,12 +85,47 @@ __device__ __forceinline__ void fwht(float (&v)[N]) {
   for (int i = 0; i < N; ++i) v[i] = __fmul_rn(v[i], c);
 }
 
-// Block c of row r (N bf16 values, 16-byte loads) as fp32.
+// A thread's row slot in shared memory: the row's D bf16 values, padded by 16 bytes so that the
+// slots of 8 consecutive threads fall on 8 different 16-byte bank groups.
+template <int D>
+struct Slots {
+  static constexpr int kPitch = D * 2 + 16;
+  static constexpr int kBytes = 2 * kThreads * kPitch;  // two rows per thread: current and next
+};
+
+// Start copying the warp's 32 rows [r0, r0 + 32) (those below `rows`) into their threads' slots
+// (slots are kPitch apart from `slots`): each copy instruction moves 32 consecutive 16-byte pieces,
+// 512 contiguous bytes of the tensor.  One commit group per call, empty or not.
+template <int D>
+__device__ __forceinline__ void fetch_rows(const __nv_bfloat16* x, long long r0, long long rows, uint32_t slots) {
+  constexpr int kPieces = D * 2 / 16;  // 16-byte pieces per row
+  const int lane = threadIdx.x & 31;
+  const char* base = reinterpret_cast<const char*>(x + r0 * D);
+#pragma unroll
+  for (int i = 0; i < kPieces; ++i) {
+    const int q = i * 32 + lane;  // piece of the warp's rows
+    const int row = q / kPieces, piece = q % kPieces;
+    if (r0 + row < rows)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(slots + row * Slots<D>::kPitch + 16 * piece),
+                   "l"(base + 16 * q)
+                   : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// All but the most recent commit group of every lane have landed and are visible to the whole warp.
+__device__ __forceinline__ void fetch_wait_prev() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+  __syncwarp();
+}
+
+// Block of N bf16 values from shared memory (16-byte loads) as fp32.
 template <int N>
-__device__ __forceinline__ void load_block(const __nv_bfloat16* src, float (&v)[N]) {
+__device__ __forceinline__ void load_block(uint32_t src, float (&v)[N]) {
 #pragma unroll
   for (int i = 0; i < N / 8; ++i) {
-    const uint4 w = reinterpret_cast<const uint4*>(src)[i];
+    uint4 w;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                 : "r"(src + 16 * i));
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -90,14 +154,24 @@ __global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const __nv_bflo
                                                                  long long rows, float* __restrict__ partial,
                                                                  long long nparts) {
   __shared__ float red[kThreads / 32];
+  extern __shared__ __align__(16) uint8_t slots_raw[];
+  const uint32_t slot0 = static_cast<uint32_t>(__cvta_generic_to_shared(slots_raw)) + threadIdx.x * Slots<D>::kPitch;
+  const uint32_t warp_slots = slot0 - (threadIdx.x & 31) * Slots<D>::kPitch;
+  const int wrow = threadIdx.x & ~31;                        // the warp's first row in a 128-row block
+  constexpr uint32_t kOther = kThreads * Slots<D>::kPitch;  // offset of the second slot
+  int cur = 0;
+  fetch_rows<D>(x, static_cast<long long>(blockIdx.x) * kRowsPerPartial + wrow, rows, warp_slots);
   for (long long pb = blockIdx.x; pb < nparts; pb += gridDim.x) {
     const long long r = pb * kRowsPerPartial + threadIdx.x;
+    fetch_rows<D>(x, (pb + gridDim.x) * kRowsPerPartial + wrow, rows, warp_slots + (cur ^ 1) * kOther);
+    fetch_wait_prev();
+    const uint32_t slot = slot0 + cur * kOther;
     float m = 0.0f;
     if (r < rows) {
 #pragma unroll 1
       for (int c = 0; c < D / N; ++c) {
         float v[N];
-        load_block<N>(x + r * D + c * N, v);
+        load_block<N>(slot + c * N * 2, v);
         fwht<N>(v);
 #pragma unroll
         for (int i = 0; i < N; ++i) m = fmaxf(m, fabsf(v[i]));
@@ -105,7 +179,9 @@ __global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const __nv_bflo
     }
     m = block_max(m, red);
     if (threadIdx.x == 0) partial[pb] = m;
+    cur ^= 1;
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // Pass 2: descale from the partial maxima, then the codes of every row.
@@ -121,28 +197,64 @@ __global__ void __launch_bounds__(kThreads) hadamard_quant_kernel(const __nv_bfl
   const float ds = amax > 0.0f ? __fdiv_rn(amax, kE4M3Max) : 1.0f;
   const float sc = amax > 0.0f ? __fdiv_rn(kE4M3Max, amax) : 1.0f;
   if (blockIdx.x == 0 && threadIdx.x == 0) *descale_out = ds;
-  for (long long pb = blockIdx.x; pb < nparts; pb += gridDim.x) {
+  extern __shared__ __align__(16) uint8_t slots_raw[];
+  const uint32_t slot0 = static_cast<uint32_t>(__cvta_generic_to_shared(slots_raw)) + threadIdx.x * Slots<D>::kPitch;
+  const uint32_t warp_slots = slot0 - (threadIdx.x & 31) * Slots<D>::kPitch;
+  const int wrow = threadIdx.x & ~31;
+  constexpr uint32_t kOther = kThreads * Slots<D>::kPitch;
+  int cur = 0;
+  fetch_rows<D>(x, static_cast<long long>(blockIdx.x) * kRowsPerPartial + wrow, rows, warp_slots);
+  for (long long pb = blockIdx.x; pb < nparts; pb += gridDim.x, cur ^= 1) {
     const long long r = pb * kRowsPerPartial + threadIdx.x;
-    if (r >= rows) continue;
+    __syncwarp();  // every lane has read the slots the next copies overwrite
+    fetch_rows<D>(x, (pb + gridDim.x) * kRowsPerPartial + wrow, rows, warp_slots + (cur ^ 1) * kOther);
+    fetch_wait_prev();
+    const uint32_t slot = slot0 + cur * kOther;
+    if (r < rows) {
 #pragma unroll 1
-    for (int c = 0; c < D / N; ++c) {
-      float v[N];
-      load_block<N>(x + r * D + c * N, v);
-      fwht<N>(v);
-      uint4* dst = reinterpret_cast<uint4*>(x8 + r * D + c * N);
+      for (int c = 0; c < D / N; ++c) {
+        float v[N];
+        load_block<N>(slot + c * N * 2, v);
+        fwht<N>(v);
+        // the codes of block c go to bytes [c N, (c + 1) N) of the slot, below the bf16 values of
+        // the blocks still to be read
 #pragma unroll
-      for (int i = 0; i < N / 16; ++i) {
-        uint32_t w[4];
+        for (int i = 0; i < N / 16; ++i) {
+          uint32_t w[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float* e = v + 16 * i + 4 * k;
-          w[k] = cvt_e4m3x2(__fmul_rn(e[1], sc), __fmul_rn(e[0], sc)) |
-                 (cvt_e4m3x2(__fmul_rn(e[3], sc), __fmul_rn(e[2], sc)) << 16);
+          for (int k = 0; k < 4; ++k) {
+            const float* e = v + 16 * i + 4 * k;
+            w[k] = cvt_e4m3x2(__fmul_rn(e[1], sc), __fmul_rn(e[0], sc)) |
+                   (cvt_e4m3x2(__fmul_rn(e[3], sc), __fmul_rn(e[2], sc)) << 16);
+          }
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + c * N + 16 * i), "r"(w[0]),
+                       "r"(w[1]), "r"(w[2]), "r"(w[3])
+                       : "memory");
         }
-        dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    __syncwarp();
+    // the warp's 32 rows of codes are contiguous in global memory: 512 bytes per store instruction
+    {
+      constexpr int kPieces = D / 16;  // 16-byte pieces of codes per row
+      const int lane = threadIdx.x & 31;
+      const long long r0 = pb * kRowsPerPartial + wrow;
+      uint8_t* base = x8 + r0 * D;
+#pragma unroll
+      for (int i = 0; i < kPieces; ++i) {
+        const int q = i * 32 + lane;
+        const int row = q / kPieces, piece = q % kPieces;
+        if (r0 + row < rows) {
+          uint4 w;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                       : "r"(warp_slots + cur * kOther + row * Slots<D>::kPitch + 16 * piece));
+          reinterpret_cast<uint4*>(base)[q] = w;
+        }
       }
     }
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 constexpr int kMaxDevices = 64;
@@ -187,13 +299,22 @@ zyfa_status_t launch_both(const void* x, void* x8, float* descale, long long row
   const long long np = num_partials(rows);
   const int nsm = sm_count();
   if (nsm <= 0) return ZYFA_ERR_CUDA;
-  const long long cap = 16ll * nsm;
+  constexpr int kSmem = Slots<D>::kBytes;
+  auto k1 = hadamard_amax_kernel<D, N>;
+  auto k2 = hadamard_quant_kernel<D, N>;
+  if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+    return ZYFA_ERR_CUDA;
+  // one wave of resident CTAs; each walks its rows with the next row's copy in flight
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k2, kThreads, kSmem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const long long cap = static_cast<long long>(per_sm) * nsm;
   const int grid = static_cast<int>(np < cap ? np : cap);
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
-  hadamard_amax_kernel<D, N><<<grid, kThreads, 0, stream>>>(xb, rows, partial, np);
+  k1<<<grid, kThreads, kSmem, stream>>>(xb, rows, partial, np);
   if (cudaGetLastError() != cudaSuccess) return ZYFA_ERR_CUDA;
-  hadamard_quant_kernel<D, N><<<grid, kThreads, 0, stream>>>(xb, rows, partial, np, static_cast<uint8_t*>(x8),
-                                                             descale);
+  k2<<<grid, kThreads, kSmem, stream>>>(xb, rows, partial, np, static_cast<uint8_t*>(x8), descale);
   return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
