@@ -246,6 +246,14 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
+__device__ __forceinline__ void unpack2(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ uint32_t cvt_relu_f16x2_pair(uint64_t t) {
   float lo, hi;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(t));
@@ -458,7 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t q_tail0 = smem_desc(s_q + C::kChunks128K * (kBlockM * 128), 16, 512, kSwizzle64B);
       const uint64_t k_desc0 = smem_desc(k_stage(0), 16, 1024, kSwizzle128B);
       const uint64_t k_tail0 = smem_desc(k_stage(0) + C::kChunks128K * (BN * 128), 16, 512, kSwizzle64B);
-      constexpr uint32_t kQTile16 = C::kQTileBytes >> 4, kStage16 = (C::kSplitKV ? C::kKStageBytes : C::kStageBytes) >> 4;
+      constexpr uint32_t kQTile16 = C::kQTileBytes >> 4;
+      constexpr uint32_t kStage16 = (C::kSplitKV ? C::kKStageBytes : C::kStageBytes) >> 4;
       uint32_t kv_cnt = 0, s_seq = 0;
       uint32_t q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
       bool ok = true;
@@ -499,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (FP8) {
             // K step ks covers keys [32ks, 32ks+32): its e8m0 scale is byte ks of the scale word
             mma_mxf8_ts(o, pa + ks * 8, vdk, idesc_block_scaled(kFmtE4M3, kFmtE4M3, true, kBlockM, C::kNO, ks, 0),
-                           tmem + C::col_sfa(t), tmem + C::kColSFB, acc);
+                        tmem + C::col_sfa(t), tmem + C::kColSFB, acc);
           } else {
             mma_f16_ts(o, pa + ks * 8, vdk, idesc_dense(kFmtBF16, kFmtBF16, false, true, kBlockM, C::kNO), acc);
           }
@@ -816,14 +825,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (kNB == 1) sfw |= sfw << 16;
         } else {
+          // packed pairs: the multiply-add and the row sum of the rounded probabilities take one
+          // instruction per two keys (the softmax warps are issue-bound)
           const float negm = -static_cast<float>(m_ref);
-          float lacc[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint64_t a2 = pack2(a, a), m2 = pack2(negm, negm);
+          uint64_t lacc[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
 #pragma unroll
           for (int i = 0; i < kPW; ++i) {
-            pw[i] = cvt_bf16x2(ex2(__fmaf_rn(s[2 * i + 1], a, negm)), ex2(__fmaf_rn(s[2 * i], a, negm)));
-            lacc[i & 3] += __uint_as_float(pw[i] << 16) + __uint_as_float(pw[i] & 0xFFFF0000u);
+            float x0, x1;
+            unpack2(ffma2(pack2(s[2 * i], s[2 * i + 1]), a2, m2), x0, x1);
+            pw[i] = cvt_bf16x2(ex2(x1), ex2(x0));
+            const uint64_t p2 = pack2(__uint_as_float(pw[i] << 16), __uint_as_float(pw[i] & 0xFFFF0000u));
+            lacc[i & 1] = fadd2(lacc[i & 1], p2);
           }
-          lsum = (lacc[0] + lacc[1]) + (lacc[2] + lacc[3]);
+          float l0, l1, l2, l3;
+          unpack2(lacc[0], l0, l1);
+          unpack2(lacc[1], l2, l3);
+          lsum = (l0 + l2) + (l1 + l3);
         }
         if (j > 0) {
           ok = mbar_wait(smem_u32(&ctl.pv_done[t]), pv_ph & 1, abort_flag, kWaitLimit);
@@ -834,7 +852,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l_bf16 = l_bf16 * f + lsum;
 #pragma unroll
-        for (int c = 0; c < kPW / 16; ++c) tmem_st16(tP + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pw + 16 * c));
+        for (int c = 0; c < kPW / 16; ++c)
+          tmem_st16(tP + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(pw + 16 * c));
         if constexpr (FP8) tmem_st4(tmem + lane_addr + C::col_sfa(t), sfw, sfw, sfw, sfw);
         if (j + 1 == ntiles) {
           tmem_wait_st();
