@@ -249,10 +249,12 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
 __device__ __forceinline__ void unpack2(uint64_t r, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
 }
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
+// lo += the low bf16 of w, hi += its high bf16 (each widened exactly, one fp32 rounding per add)
+__device__ __forceinline__ void add_bf16x2(uint32_t w, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %0;\n\t"
+      "add.rn.f32.bf16 %1, h, %1;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(w));
 }
 __device__ __forceinline__ uint32_t cvt_relu_f16x2_pair(uint64_t t) {
   float lo, hi;
@@ -825,22 +827,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (kNB == 1) sfw |= sfw << 16;
         } else {
-          // packed pairs: the multiply-add and the row sum of the rounded probabilities take one
-          // instruction per two keys (the softmax warps are issue-bound)
+          // the softmax warps are issue-bound: the multiply-add takes one packed instruction per two
+          // keys, and the row sum adds each rounded bf16 probability straight into an fp32
+          // accumulator (four of them: even / odd keys of even / odd words)
           const float negm = -static_cast<float>(m_ref);
           const uint64_t a2 = pack2(a, a), m2 = pack2(negm, negm);
-          uint64_t lacc[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
+          float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
           for (int i = 0; i < kPW; ++i) {
             float x0, x1;
             unpack2(ffma2(pack2(s[2 * i], s[2 * i + 1]), a2, m2), x0, x1);
             pw[i] = cvt_bf16x2(ex2(x1), ex2(x0));
-            const uint64_t p2 = pack2(__uint_as_float(pw[i] << 16), __uint_as_float(pw[i] & 0xFFFF0000u));
-            lacc[i & 1] = fadd2(lacc[i & 1], p2);
+            if (i & 1) add_bf16x2(pw[i], l2, l3);
+            else add_bf16x2(pw[i], l0, l1);
           }
-          float l0, l1, l2, l3;
-          unpack2(lacc[0], l0, l1);
-          unpack2(lacc[1], l2, l3);
           lsum = (l0 + l2) + (l1 + l3);
         }
         if (j > 0) {
