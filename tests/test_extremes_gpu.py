@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle as O
-from _gpu_util import FP8_TOL, oracle_out, per_row_rel, select, to_device
+from _gpu_util import BF16_TOL, FP8_TOL, oracle_out, per_row_rel, run_gpu, select, to_device
 from fp8_causal_prefill_gb300 import flash_attn_func, zyfa_check_errors
 from fp8_causal_prefill_gb300.inputs import Shape, make_problem, sample_rows
 
@@ -46,3 +46,18 @@ def test_extreme_score_range(p_mode):
     got = select(out)
     assert np.all(np.isfinite(got))
     assert O.rel_l2(got, ref) <= FP8_TOL
+
+
+def test_extreme_score_range_bf16():
+    # q scaled by 40 (re-rounded to bf16): scores spread over hundreds of binades per row, so the row
+    # reference rises many times (conditional rescales of O and l) and most probabilities underflow;
+    # the device flushes results below 2^-126 to zero, the oracle keeps bf16 subnormals down to 2^-133,
+    # a difference of at most 2^-126 of the row's largest weight
+    sh = Shape(1, 700, 2, 1, 128, 128)
+    p = make_problem(sh, seed=33)
+    p.qb = (p.qb.float() * 40.0).to(torch.bfloat16)
+    out = run_gpu(p, "bf16")
+    assert zyfa_check_errors() == 0
+    got = select(out)
+    assert np.all(np.isfinite(got))
+    assert O.rel_l2(got, oracle_out(p, "bf16")) <= BF16_TOL
