@@ -1,6 +1,6 @@
 """GPU parity of the Hadamard pre-pass (zyfa_hadamard_quantize_e4m3) with its oracle: codes and
-descale bit for bit (both sides rotate in float32 in the same stage order and quantise with the same
-fp32 division and e4m3 rounding), and attention on rotated inputs."""
+descale bit for bit (both sides rotate in float32 in the same stage order, multiply every rotated
+value by the same fp32 scale fl32(448/amax) and round to e4m3), and attention on rotated inputs."""
 import math
 
 import numpy as np

@@ -415,3 +415,59 @@ def test_lse_of_block_scaled_paths_within_rounding_bounds_of_exact():
     assert np.max(np.abs(l2 - l1)) <= -math.log1p(-PAGE["leanp_max_rel_error"])
     assert np.max(np.abs(lx - l1)) <= -math.log1p(-PAGE["exact_rounding_max_rel_error"])
     assert np.max(np.abs(l2 - l1)) > 1e-4          # the rounding is visible, not skipped
+
+
+# ----------------------------------------------------------------------------------------------
+# O4's rounding of each probability to bfloat16 and O2's e8m0 range, against closed forms
+
+
+def _unit_bf16_scale():
+    """The fp32 softmax scale whose fl32(scale * fl32(log2 e)) is exactly 1, so x = raw score."""
+    sc = float(np.float32(np.float32(1.0) / np.float32(O.attention.LOG2E_F32)))
+    assert O.bf16_score_scale(sc) == 1.0
+    return sc
+
+
+def test_bf16_twin_rounds_each_probability_to_bf16_and_uses_an_integer_reference():
+    # Three rows whose scores (in binades, a' = 1) are bf16 numbers chosen so that each probability
+    # 2^(x - M) falls between two bf16 values:
+    #   row 1: x = [0, -127/128]: M = 0; 2^(-127/128) = 0.50271... lies between 128/256 and 129/256,
+    #          nearer 129/256, so p = [1, 129/256] and with v = [0, 1] the output is 129/385;
+    #   row 2: x = [-1/4, -5/4, -3]: M = ceil(-1/4) = 0 (an integer, not the row maximum);
+    #          2^(-1/4) = 0.84089... -> 215/256, 2^(-5/4) = 0.42044... -> 215/512, 2^-3 = 1/8, so with
+    #          v = [0, 1, 2] the output is (215/512 + 2/8) / (215/256 + 215/512 + 1/8) = 343/709.
+    # Rounding p to fp32 instead, or taking M = max x, moves both outputs by more than 1e-4.
+    assert 128.5 / 256 < 2 ** (-127 / 128) < 129 / 256
+    assert 214.5 / 256 < 2 ** -0.25 < 215.5 / 256 and 214.5 / 512 < 2 ** -1.25 < 215.5 / 512
+    sc = _unit_bf16_scale()
+    d = 16
+    q = np.zeros((1, 3, 1, d))
+    q[0, 0, 0, 0] = q[0, 1, 0, 0] = 1.0      # rows 0 and 1 read channel 0 of the keys
+    q[0, 2, 0, 1] = 1.0                      # row 2 reads channel 1
+    k = np.zeros((1, 3, 1, d))
+    k[0, :, 0, 0] = [0.0, -127 / 128, 0.0]
+    k[0, :, 0, 1] = [-0.25, -1.25, -3.0]
+    v = np.zeros((1, 3, 1, 8))
+    v[0, :, 0, 0] = [0.0, 1.0, 2.0]
+    v[0, :, 0, 1] = 1.0
+    assert np.array_equal(O.bf16_round(np.concatenate([q.ravel(), k.ravel(), v.ravel()])),
+                          np.concatenate([q.ravel(), k.ravel(), v.ravel()]))
+    out = O.bf16_causal_attention(q, k, v, sc)
+    assert out[0, 0, 0, 0] == 0.0
+    assert abs(out[0, 1, 0, 0] - 129 / 385) < 1e-15
+    assert abs(out[0, 2, 0, 0] - 343 / 709) < 1e-15
+    np.testing.assert_allclose(out[0, :, 0, 1], 1.0, rtol=0, atol=1e-15)
+
+
+def test_leanp_weight_is_dropped_beyond_the_e8m0_range():
+    # Two 64-key blocks; the second lies 126, 127 or 130 binades below the first (a = 8, so the raw
+    # score is in binades and e = ceil(score)).  Its codes are all 56 (probability 1 within the
+    # block), so its weight is 2^(e_2 - e_1): kept at 2^-126, the end of the e8m0 scale range, and 0
+    # beyond it.
+    for below, expect in ((126, 2.0 ** -126), (127, 0.0), (130, 0.0)):
+        s = np.zeros((1, 128))
+        s[0, 64:] = -float(below)
+        code, e, w = O.leanp_row_weights(s, 8.0)
+        assert list(e[0]) == [0.0, -float(below)]
+        assert np.all(code == 56) and np.all(w[0, :64] == 1.0)
+        assert np.all(w[0, 64:] == expect), (below, w[0, 64])
