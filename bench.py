@@ -5,6 +5,7 @@ One step = one zyfa_attn_fwd_causal call over the whole workload B=1, H=32, H_kv
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--dtype fp8|bf16] [--config bench32k|mla32k|...]
   python bench.py --impl reference ...     # the CPU oracle on the host cores, same metric and workload
+  python bench.py --mma-rate               # the GPU's dense FP8 / BF16 tensor-core rate (the peak's measurement)
 
 FLOP convention: ``value`` counts the algorithmic causal FLOPs B*H*S^2*(D_qk+D_v) (half the dense count,
 what the tensor cores must execute); ``value_dense_formula`` reports the 2*B*H*S^2*(D_qk+D_v) variant.
@@ -48,6 +49,8 @@ def parse():
                     help="also time the Hadamard rotation + quantisation pre-pass of Q and K (bf16 in)")
     ap.add_argument("--p-mode", choices=["lean", "exact"], default="lean",
                     help="FP8 probabilities: Lean P (the method) or exact exponential (the ablation)")
+    ap.add_argument("--mma-rate", action="store_true",
+                    help="measure the dense FP8 and BF16 tcgen05 MMA rate (burst and sustained) instead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--host-chunks", type=int, default=0,
                     help="chunks of the host-buffer call in the e2e leg (0 = the library default, 4)")
@@ -262,12 +265,79 @@ def run_reference(args):
     return 0
 
 
+def run_mma_rate(args):
+    """Dense tensor-core rate of this GPU with the attention kernel's MMA forms: one CTA per SM issuing
+    M=128, N=256 MMAs from shared memory (zyfa_probe_mma_rate).  A burst of ten launches and a loop of
+    at least three seconds (where the board's power cap sets the clock); CUDA events for the rate,
+    each CTA's clock64 span for FLOP per cycle per SM."""
+    import torch
+
+    from fp8_causal_prefill_gb300 import api
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib = api.load_library()
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    smi_index = 0
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    if visible and visible[0].strip().isdigit():
+        smi_index = int(visible[0])
+    line = {"probe": "dense tcgen05 MMA rate, M=128 N=256, operands in shared memory, one CTA per SM",
+            "sms": nsm}
+    for name, fp8, iters in (("fp8_e4m3", 1, 20000), ("bf16", 0, 10000)):
+        fpi = lib.zyfa_probe_mma_flops_per_iter(fp8)
+        cycles = torch.zeros(nsm, dtype=torch.int64, device=dev)
+        flag = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def launch():
+            st = lib.zyfa_probe_mma_rate(fp8, iters, nsm, cycles.data_ptr(), flag.data_ptr(), sptr)
+            if st != 0:
+                raise api.ZyfaError(st, "zyfa_probe_mma_rate")
+        for _ in range(3):
+            launch()
+        torch.cuda.synchronize(dev)
+        res = {}
+        for mode, n in (("burst", 10), ("sustained", None)):
+            sampler = ClockSampler(smi_index)
+            sampler.start()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if n is None:   # enough launches for about three seconds at the burst rate
+                n = max(10, int(3.0 / (res["burst_ms_per_launch"] * 1e-3)))
+            t0 = time.time()
+            e0.record(stream)
+            for _ in range(n):
+                launch()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            sampler.mark(t0, time.time())
+            clk = sampler.stop()
+            ms = e0.elapsed_time(e1) / n
+            cyc = int(cycles.max().item())
+            res[f"{mode}_ms_per_launch"] = ms
+            res[f"{mode}_tflops"] = fpi * iters * nsm / (ms * 1e-3) / 1e12
+            res[f"{mode}_launches"] = n
+            res[f"{mode}_sm_mhz"] = clk.get("sm_mhz")
+            res[f"{mode}_clock_reasons"] = clk.get("reasons")
+            res[f"{mode}_flop_per_cycle_per_sm"] = fpi * iters / cyc
+        if int(flag.item()) != 0:
+            res["timed_out"] = True
+        fpc = res["burst_flop_per_cycle_per_sm"]
+        res["tflops_at_2070_mhz"] = fpc * nsm * 2070e6 / 1e12
+        line[name] = res
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     import numpy as np
 
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.mma_rate:
+        return run_mma_rate(args)
 
     import torch
     import torch.distributed as dist

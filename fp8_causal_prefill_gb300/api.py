@@ -24,7 +24,8 @@ STATUS = {0: "ZYFA_OK", 1: "ZYFA_ERR_INVALID_ARG", 2: "ZYFA_ERR_UNSUPPORTED", 3:
 EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_attn_fwd_causal_ex", "zyfa_attn_fwd_causal_host", "zyfa_check_errors",
             "zyfa_status_string",
             "zyfa_kernel_launches", "zyfa_selftest_stalled_pipeline", "zyfa_hadamard_quantize_e4m3",
-            "zyfa_hadamard_quantize_e4m3_noalloc", "zyfa_hadamard_workspace_bytes")
+            "zyfa_hadamard_quantize_e4m3_noalloc", "zyfa_hadamard_workspace_bytes", "zyfa_probe_mma_rate",
+            "zyfa_probe_mma_flops_per_iter")
 ZYFA_P_LEAN = 0
 ZYFA_P_EXACT = 1
 
@@ -77,6 +78,10 @@ def load_library() -> ctypes.CDLL:
         lib.zyfa_status_string.restype = ctypes.c_char_p
         lib.zyfa_kernel_launches.argtypes = [ci, ci, ci]
         lib.zyfa_kernel_launches.restype = ci
+        lib.zyfa_probe_mma_rate.argtypes = [ci, ci, ci, vp, vp, vp]
+        lib.zyfa_probe_mma_rate.restype = ci
+        lib.zyfa_probe_mma_flops_per_iter.argtypes = [ci]
+        lib.zyfa_probe_mma_flops_per_iter.restype = ll
         _lib = lib
         return lib
 

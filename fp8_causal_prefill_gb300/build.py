@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzyfa.so")
 SOURCES = ["zyfa_api.cu", "zyfa_kernels_fp8.cu", "zyfa_kernels_fp8_exact.cu", "zyfa_kernels_bf16.cu",
-           "zyfa_hadamard.cu"]
+           "zyfa_hadamard.cu", "zyfa_probe.cu"]
 # The attention kernel splits its registers between warpgroups at run time (setmaxnreg); the split is
 # sized for exactly this many registers per thread at launch, which every instantiation must get.
 KERNEL_REGS = 168

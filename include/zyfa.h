@@ -221,6 +221,28 @@ const char* zyfa_status_string(zyfa_status_t status);
  */
 int zyfa_kernel_launches(int B, int S, int H);
 
+/*
+ * zyfa_probe_mma_rate - measure this GPU's dense tensor-core rate with the attention kernel's own
+ * instruction forms (the denominator of "% of FP8 peak"; captivela ZYFA article, "Angka Nyata",
+ * quotes FP8 prefill throughput as a share of the FP8 peak).
+ *
+ *   fp8        1: tcgen05.mma kind::f8f6f4 on e4m3 operands; 0: kind::f16 on bf16 operands.
+ *   iters      MMA iterations per CTA (>= 1); one iteration is zyfa_probe_mma_flops_per_iter(fp8)
+ *              floating-point operations (an M=128, N=256 product over 128 bytes of K).
+ *   grid       CTAs to launch; one CTA occupies one SM (pass the SM count to load every SM).
+ *   cycles     device array of `grid` long longs: each CTA's clock64 span from its first MMA issue
+ *              to the completion of its last MMA.
+ *   timed_out  device int; bit 0 is set if a CTA gave up waiting (a few seconds) for its MMAs.
+ * Asynchronous on `stream`; the caller times the launch (CUDA events) and owns both buffers.  The
+ * operands are synthetic values held in shared memory; nothing else is read or written.  Returns
+ * ZYFA_ERR_INVALID_ARG for bad arguments, ZYFA_ERR_CUDA if the launch fails.
+ */
+zyfa_status_t zyfa_probe_mma_rate(int fp8, int iters, int grid, long long* cycles, int* timed_out,
+                                  cudaStream_t stream);
+
+/* zyfa_probe_mma_flops_per_iter - floating-point operations of one probe iteration per CTA. */
+long long zyfa_probe_mma_flops_per_iter(int fp8);
+
 #ifdef __cplusplus
 }
 #endif
