@@ -43,8 +43,9 @@ def parse():
     ap.add_argument("--config", default="bench32k")
     ap.add_argument("--heads", type=int, default=0, help="override H (profiling a smaller case)")
     ap.add_argument("--seq", type=int, default=0, help="override S (a sequence-length sweep)")
-    ap.add_argument("--energy", action="store_true",
-                    help="also measure energy per step (NVML total-energy counter over a >= 2 s loop)")
+    ap.add_argument("--no-energy", action="store_true",
+                    help="skip the energy record (NVML total-energy counter around a loop of >= --energy-seconds)")
+    ap.add_argument("--energy-seconds", type=float, default=1.0)
     ap.add_argument("--hadamard", action="store_true",
                     help="also time the Hadamard rotation + quantisation pre-pass of Q and K (bf16 in)")
     ap.add_argument("--p-mode", choices=["lean", "exact"], default="lean",
@@ -95,42 +96,162 @@ def workload_name(sh, dtype, p_mode="lean"):
             f"D_qk={sh.D_qk} D_v={sh.D_v} {sh.kind} inputs{extra}")
 
 
+NVML_CLOCK_SM = 1
+# clock event (throttle) reason bits of NVML's public API that bear on a measurement
+NVML_REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
+
+
+def _device_uuid(dev_index):
+    try:
+        import torch
+        if torch.cuda.is_available():
+            u = getattr(torch.cuda.get_device_properties(dev_index), "uuid", None)
+            return None if u is None else str(u)
+    except Exception:  # noqa: BLE001 - no device, no uuid: fall back to the index
+        pass
+    return None
+
+
+class Nvml:
+    """Read-only NVML queries for one GPU through ctypes: SM clock, maximum SM clock, board power,
+    clock event reasons and the cumulative board energy.  Nothing is set.  ``lib`` replaces
+    libnvidia-ml (tests pass a fake); ``ok`` is False when NVML cannot be used."""
+
+    def __init__(self, cuda_index, nvml_index=None, lib=None):
+        import ctypes
+        self.c = ctypes
+        self.lib = None
+        self.h = ctypes.c_void_p()
+        try:
+            lib = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            # the CUDA device's UUID names the same board in NVML; the index is the fallback
+            uuid = _device_uuid(cuda_index)
+            ok = uuid is not None and lib.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(),
+                                                                      ctypes.byref(self.h)) == 0
+            if not ok:
+                idx = cuda_index if nvml_index is None else nvml_index
+                ok = lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.h)) == 0
+            if ok:
+                self.lib = lib
+        except (OSError, AttributeError):
+            self.lib = None
+
+    @property
+    def ok(self):
+        return self.lib is not None
+
+    def _query(self, fn_names, ctype, *args):
+        if self.lib is None:
+            return None
+        for name in fn_names:
+            fn = getattr(self.lib, name, None)
+            if fn is None:
+                continue
+            v = ctype(0)
+            return int(v.value) if fn(self.h, *args, self.c.byref(v)) == 0 else None
+        return None
+
+    def sm_mhz(self):
+        return self._query(("nvmlDeviceGetClockInfo",), self.c.c_uint, NVML_CLOCK_SM)
+
+    def sm_max_mhz(self):
+        return self._query(("nvmlDeviceGetMaxClockInfo",), self.c.c_uint, NVML_CLOCK_SM)
+
+    def power_w(self):
+        mw = self._query(("nvmlDeviceGetPowerUsage",), self.c.c_uint)
+        return None if mw is None else mw / 1000.0
+
+    def reasons_mask(self):
+        return self._query(("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"),
+                           self.c.c_ulonglong)
+
+    def energy_mj(self):
+        return self._query(("nvmlDeviceGetTotalEnergyConsumption",), self.c.c_ulonglong)
+
+
 class EnergyCounter:
     """Cumulative board energy of one GPU from NVML (read only), millijoules."""
 
-    def __init__(self, dev_index):
-        import ctypes
-        self.c = ctypes
-        self.nvml = None
-        self.h = ctypes.c_void_p()
-        try:
-            nvml = ctypes.CDLL("libnvidia-ml.so.1")
-            if nvml.nvmlInit_v2() != 0:
-                return
-            import torch
-            uuid = getattr(torch.cuda.get_device_properties(dev_index), "uuid", None)
-            ok = False
-            if uuid is not None:
-                ok = nvml.nvmlDeviceGetHandleByUUID(("GPU-" + str(uuid)).encode(), ctypes.byref(self.h)) == 0
-            if not ok:
-                ok = nvml.nvmlDeviceGetHandleByIndex_v2(dev_index, ctypes.byref(self.h)) == 0
-            if ok:
-                self.nvml = nvml
-        except OSError:
-            self.nvml = None
+    def __init__(self, cuda_index, nvml_index=None, lib=None):
+        self.nvml = Nvml(cuda_index, nvml_index, lib)
 
     def read_mj(self):
-        if self.nvml is None:
-            return None
-        e = self.c.c_ulonglong(0)
-        if self.nvml.nvmlDeviceGetTotalEnergyConsumption(self.h, self.c.byref(e)) != 0:
-            return None
-        return int(e.value)
+        return self.nvml.energy_mj()
+
+
+def energy_block(e_start_mj, e_end_mj, steps, flops_per_step, seconds):
+    """Energy per step and TFLOP per joule from two readings of the cumulative energy counter around
+    `steps` steps that took `seconds`; an `unavailable` record when the counter gave nothing usable."""
+    if e_start_mj is None or e_end_mj is None or e_end_mj <= e_start_mj or steps <= 0 or seconds <= 0:
+        return {"unavailable": "NVML energy counter not readable on this box"}
+    joules = (e_end_mj - e_start_mj) * 1e-3
+    return {"joules_per_step": joules / steps, "tflop_per_joule": flops_per_step * steps / joules / 1e12,
+            "avg_power_w": joules / seconds, "steps": steps, "seconds": seconds,
+            "method": "NVML total-energy counter (board), read before and after the loop"}
+
+
+def summarize_clocks(rows, window, source):
+    """Clock record of a timed region from samples (wall time, SM MHz, max SM MHz, power W or None,
+    set of active reason names): only samples inside the window count, unless there are none."""
+    inside = [r for r in rows if window and window[0] <= r[0] <= window[1]]
+    used = inside if inside else rows
+    reasons = set().union(*[r[4] for r in used]) if used else set()
+    sm = [r[1] for r in used]
+    power = [r[3] for r in used if r[3] is not None]
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_mhz_min": min(sm) if sm else None,
+            "sm_max_mhz": max(r[2] for r in used) if used else None,
+            "power_w_median": statistics.median(power) if power else None, "samples": len(sm),
+            "samples_in_window": bool(inside), "reasons": sorted(reasons), "source": source}
+
+
+class NvmlSampler:
+    """SM clock, power and clock event reasons from NVML every `period` seconds on a host thread
+    (read-only queries); only samples stamped inside the timed region are summarised."""
+
+    def __init__(self, nvml, period=0.005):
+        self.nvml = nvml
+        self.period = period
+        self.rows = []
+        self.window = None
+        self._stop = None
+        self._thread = None
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def sample(self):
+        sm = self.nvml.sm_mhz()
+        if sm is None:
+            return
+        mask = self.nvml.reasons_mask() or 0
+        names = {n for n, bit in NVML_REASONS.items() if mask & bit}
+        self.rows.append((time.time(), float(sm), float(self.nvml.sm_max_mhz() or 0), self.nvml.power_w(), names))
+
+    def start(self):
+        import threading
+        self._stop = threading.Event()
+
+        def run():
+            while not self._stop.is_set():
+                self.sample()
+                self._stop.wait(self.period)
+        self._thread = threading.Thread(target=run, daemon=True)
+        self._thread.start()
+        time.sleep(0.05)
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        return summarize_clocks(self.rows, self.window, f"NVML every {self.period * 1e3:g} ms")
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 50 ms; only samples stamped inside the timed region (host wall clock,
-    from the launch of the first timed step to the synchronize after the last) are summarised."""
+    """nvidia-smi sampled every 50 ms (used when NVML cannot be loaded in-process); only samples stamped
+    inside the timed region (host wall clock, from the launch of the first timed step to the
+    synchronize after the last) are summarised."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw.instant,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -181,16 +302,10 @@ class ClockSampler:
                 pw = None
             rows.append((ts, vals[0], vals[1], pw, parts[5:9]))
         os.unlink(self.path)
-        inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
-        used = inside if inside else rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = {n for r in used for n, v in zip(names, r[4]) if v.lower().startswith("active")}
-        sm = [r[1] for r in used]
-        power = [r[3] for r in used if r[3] is not None]
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_mhz_min": min(sm) if sm else None,
-                "sm_max_mhz": max(r[2] for r in used) if used else None,
-                "power_w_median": statistics.median(power) if power else None, "samples": len(sm),
-                "samples_in_window": bool(inside), "reasons": sorted(reasons)}
+        rows = [(r[0], r[1], r[2], r[3], {n for n, v in zip(names, r[4]) if v.lower().startswith("active")})
+                for r in rows]
+        return summarize_clocks(rows, self.window, "nvidia-smi every 50 ms")
 
 
 def slowest_rank_ms(local_ms: float, world: int, device) -> float:
@@ -265,6 +380,12 @@ def run_reference(args):
     return 0
 
 
+def make_sampler(cuda_index, nvml_index):
+    """The clock record's sampler: NVML in-process every 5 ms, else nvidia-smi every 50 ms."""
+    nv = Nvml(cuda_index, nvml_index)
+    return NvmlSampler(nv) if nv.ok else ClockSampler(nvml_index)
+
+
 def run_mma_rate(args):
     """Dense tensor-core rate of this GPU with the attention kernel's MMA forms: one CTA per SM issuing
     M=128, N=256 MMAs from shared memory (zyfa_probe_mma_rate).  A burst of ten launches and a loop of
@@ -300,7 +421,7 @@ def run_mma_rate(args):
         torch.cuda.synchronize(dev)
         res = {}
         for mode, n in (("burst", 10), ("sustained", None)):
-            sampler = ClockSampler(smi_index)
+            sampler = make_sampler(0, smi_index)
             sampler.start()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             if n is None:   # enough launches for about three seconds at the burst rate
@@ -394,7 +515,7 @@ def main():
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     if local < len(visible) and visible[local].strip().isdigit():
         smi_index = int(visible[local])
-    sampler = ClockSampler(smi_index)
+    sampler = make_sampler(local, smi_index) if rank == 0 else None
     if rank == 0:
         sampler.start()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -413,8 +534,10 @@ def main():
         step(dq, dk, dv, out)
         ends[i].record(stream)
     barrier()
-    sampler.mark(t_wall0, time.time())
-    clocks = sampler.stop() if rank == 0 else None
+    clocks = None
+    if rank == 0:
+        sampler.mark(t_wall0, time.time())
+        clocks = sampler.stop()
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(kernel_ms) if flush else starts[0].elapsed_time(ends[-1])
     ms_per_step = slowest_rank_ms(total_ms, world, dev) / args.steps
@@ -423,11 +546,12 @@ def main():
     if zst != 0:
         raise api.ZyfaError(zst, "kernel status")
 
-    # energy per step: NVML's cumulative energy counter around a loop of at least two seconds
+    # energy per step: NVML's cumulative energy counter (read only) around a loop of at least
+    # --energy-seconds (the counter moves in steps too coarse for a window of a few milliseconds)
     energy = None
-    if args.energy and rank == 0:
-        meter = EnergyCounter(local)
-        n_en = max(args.steps, int(2.0 / max(ms_per_step * 1e-3, 1e-6)) + 1)
+    if not args.no_energy and rank == 0:
+        meter = EnergyCounter(local, smi_index)
+        n_en = max(args.steps, int(args.energy_seconds / max(ms_per_step * 1e-3, 1e-6)) + 1)
         e_start = meter.read_mj()
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         g0.record(stream)
@@ -435,15 +559,7 @@ def main():
             step(dq, dk, dv, out)
         g1.record(stream)
         torch.cuda.synchronize(dev)
-        e_end = meter.read_mj()
-        secs = g0.elapsed_time(g1) * 1e-3
-        if e_start is not None and e_end is not None and e_end > e_start:
-            joules = (e_end - e_start) * 1e-3
-            energy = {"joules_per_step": joules / n_en, "tflop_per_joule": flops * n_en / joules / 1e12,
-                      "avg_power_w": joules / secs, "steps": n_en, "seconds": secs,
-                      "method": "NVML total-energy counter (board), read before and after the loop"}
-        else:
-            energy = {"unavailable": "NVML energy counter not readable on this box"}
+        energy = energy_block(e_start, meter.read_mj(), n_en, flops, g0.elapsed_time(g1) * 1e-3)
 
     # the Hadamard pre-pass of Q and K (bf16 -> rotated e4m3 + descale), timed on its own
     prepass = None
@@ -559,6 +675,9 @@ def main():
             "gpu_launches": args.steps * api.zyfa_kernel_launches(sh.B, sh.S, sh.H),
             "clocks": clocks,
         }
+        if clocks is not None and clocks.get("sm_mhz"):
+            # step time x median SM clock: the step in thousands of SM cycles, comparable across clocks
+            clocks["kcycles_per_step"] = ms_per_step * clocks["sm_mhz"]
         if e2e is not None:
             line["e2e"] = e2e
         if prepass is not None:

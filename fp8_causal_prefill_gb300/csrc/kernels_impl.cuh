@@ -1,5 +1,8 @@
 // Launch wrapper shared by the FP8 and BF16 kernel translation units.
 #pragma once
+#include <atomic>
+#include <cstdint>
+
 #include "launch.h"
 #include "zyfa_fwd.cuh"
 
@@ -20,8 +23,17 @@ cudaError_t launch_fwd(const LaunchArgs& a) {
   constexpr int BN = tile_keys<FP8, DQK, DV>();
   using C = Cfg<FP8, DQK, DV, BN>;
   auto kernel = zyfa_fwd_kernel<FP8, DQK, DV, BN, EXACT>;
-  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (err != cudaSuccess) return err;
+  // the shared-memory opt-in is an attribute of the function on the current device: set it once per
+  // device (a host-side cost of several microseconds that short launches would otherwise pay)
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+  if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
+    const cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr_set.fetch_or(bit, std::memory_order_acq_rel);
+  }
   Params p;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.q_descale = a.q_descale;
