@@ -5,5 +5,6 @@ The compute path is the C-ABI library ``libzyfa.so`` built from ``csrc/`` for sm
 only marshals arguments to it.  Importing the package does not load the library: the first call
 does, and it raises if the library is missing.
 """
-from .api import (ZyfaError, flash_attn_func, hadamard_quantize_e4m3, library_path, load_library,  # noqa: F401
-                  zyfa_attn_fwd_causal, zyfa_attn_fwd_causal_ex, zyfa_check_errors, zyfa_kernel_launches)
+from .api import (ZyfaError, flash_attn_func, hadamard_quantize_e4m3, hadamard_quantize_qk_e4m3,  # noqa: F401
+                  library_path, load_library, zyfa_attn_fwd_causal, zyfa_attn_fwd_causal_ex, zyfa_check_errors,
+                  zyfa_kernel_launches)

@@ -24,7 +24,8 @@ STATUS = {0: "ZYFA_OK", 1: "ZYFA_ERR_INVALID_ARG", 2: "ZYFA_ERR_UNSUPPORTED", 3:
 EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_attn_fwd_causal_ex", "zyfa_attn_fwd_causal_host", "zyfa_check_errors",
             "zyfa_status_string",
             "zyfa_kernel_launches", "zyfa_selftest_stalled_pipeline", "zyfa_hadamard_quantize_e4m3",
-            "zyfa_hadamard_quantize_e4m3_noalloc", "zyfa_hadamard_workspace_bytes", "zyfa_probe_mma_rate",
+            "zyfa_hadamard_quantize_e4m3_noalloc", "zyfa_hadamard_quantize_qk_e4m3", "zyfa_hadamard_workspace_bytes",
+            "zyfa_probe_mma_rate",
             "zyfa_probe_mma_flops_per_iter")
 ZYFA_P_LEAN = 0
 ZYFA_P_EXACT = 1
@@ -68,6 +69,8 @@ def load_library() -> ctypes.CDLL:
         ll, sz = ctypes.c_longlong, ctypes.c_size_t
         lib.zyfa_hadamard_quantize_e4m3.argtypes = [vp, vp, vp, ll, ci, vp, sz, vp]
         lib.zyfa_hadamard_quantize_e4m3.restype = ci
+        lib.zyfa_hadamard_quantize_qk_e4m3.argtypes = [vp, vp, vp, ll, vp, vp, vp, ll, ci, vp, sz, vp]
+        lib.zyfa_hadamard_quantize_qk_e4m3.restype = ci
         lib.zyfa_hadamard_quantize_e4m3_noalloc.argtypes = [vp, vp, vp, ll, ci, vp]
         lib.zyfa_hadamard_quantize_e4m3_noalloc.restype = ci
         lib.zyfa_hadamard_workspace_bytes.argtypes = [ll]
@@ -215,6 +218,15 @@ def zyfa_hadamard_quantize_e4m3_noalloc(x: int, x8: int, descale: int, rows: int
                                                              stream or None)
 
 
+def zyfa_hadamard_quantize_qk_e4m3(q: int, q8: int, q_descale: int, q_rows: int, k: int, k8: int, k_descale: int,
+                                   k_rows: int, D: int, workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    """Call the C pre-pass for Q and K together (one launch per pass) with raw addresses; returns the
+    status code."""
+    return load_library().zyfa_hadamard_quantize_qk_e4m3(q or None, q8 or None, q_descale or None, q_rows, k or None,
+                                                         k8 or None, k_descale or None, k_rows, D, workspace or None,
+                                                         workspace_bytes, stream or None)
+
+
 def zyfa_hadamard_workspace_bytes(rows: int) -> int:
     return load_library().zyfa_hadamard_workspace_bytes(rows)
 
@@ -237,3 +249,29 @@ def hadamard_quantize_e4m3(x: torch.Tensor):
     if st != 0:
         raise ZyfaError(st, "zyfa_hadamard_quantize_e4m3")
     return codes.view(torch.float8_e4m3fn), descale
+
+
+def hadamard_quantize_qk_e4m3(q: torch.Tensor, k: torch.Tensor):
+    """Rotate and quantise Q and K together (contiguous bf16 CUDA tensors with the same last dimension
+    D): one launch per pass for both.  Returns (q codes, q descale, k codes, k descale) as
+    hadamard_quantize_e4m3 does for each."""
+    for t in (q, k):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError("q and k must be contiguous bfloat16 CUDA tensors")
+    D = q.shape[-1]
+    if k.shape[-1] != D or k.device != q.device:
+        raise ValueError("q and k need the same head dimension and device")
+    qr, kr = (q.numel() // D if D else 0), (k.numel() // D if D else 0)
+    q8 = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
+    k8 = torch.empty(k.shape, dtype=torch.uint8, device=q.device)
+    ds = torch.ones(2, dtype=torch.float32, device=q.device)
+    nbytes = zyfa_hadamard_workspace_bytes(qr) + zyfa_hadamard_workspace_bytes(kr)
+    ws = torch.empty(max(1, nbytes // 4), dtype=torch.float32, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = zyfa_hadamard_quantize_qk_e4m3(q.data_ptr(), q8.data_ptr(), ds.data_ptr(), qr, k.data_ptr(),
+                                            k8.data_ptr(), ds.data_ptr() + 4, kr, D, ws.data_ptr(), ws.numel() * 4,
+                                            stream)
+    if st != 0:
+        raise ZyfaError(st, "zyfa_hadamard_quantize_qk_e4m3")
+    return q8.view(torch.float8_e4m3fn), ds[0:1], k8.view(torch.float8_e4m3fn), ds[1:2]

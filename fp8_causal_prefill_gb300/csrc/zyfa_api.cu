@@ -262,7 +262,14 @@ zyfa_status_t zyfa_attn_fwd_causal_host(const void* q_host, const void* k_host, 
   if (!shape_ok) return ZYFA_ERR_UNSUPPORTED;
   if (S == 0) return ZYFA_OK;
   if (!q_host || !k_host || !v_host || !out_host) return ZYFA_ERR_INVALID_ARG;
+  // the checks the kernel launches would make, before any copy is enqueued: an argument error
+  // leaves every buffer and stream untouched
+  if (!q_dev || !k_dev || !v_dev || !out_dev) return ZYFA_ERR_INVALID_ARG;
+  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if (misaligned(q_dev) || misaligned(k_dev) || misaligned(v_dev) || misaligned(out_dev)) return ZYFA_ERR_MISALIGNED;
+  if (!std::isfinite(softmax_scale) || softmax_scale < 0.0f) return ZYFA_ERR_INVALID_ARG;
   const long long nqb = (static_cast<long long>(S) + kUnitRows - 1) / kUnitRows;
+  if (nqb * B * H > (1ll << 30) || static_cast<long long>(S) > (1ll << 30)) return ZYFA_ERR_UNSUPPORTED;
   if (chunks == 0) chunks = 4;
   if (chunks > nqb) chunks = static_cast<int>(nqb);
   if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;

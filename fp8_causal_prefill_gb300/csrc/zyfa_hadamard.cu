@@ -11,8 +11,12 @@
 // The per-tensor maximum needs a pass over the whole tensor before any code can be written, so the
 // work is two launches over the same rows: pass 1 rotates and writes one partial maximum per block of
 // 128 rows into scratch memory, pass 2 reduces those partials to the descale, rotates again and
-// writes the codes.  The scratch is caller-provided workspace (zyfa_hadamard_quantize_e4m3) or a
-// fixed array inside this library (zyfa_hadamard_quantize_e4m3_noalloc).
+// writes the codes.  One launch of each pass can cover two tensors (Q and K, which share the head
+// dimension): their 128-row blocks are numbered one after the other, each tensor keeps its own
+// maximum, and the grid's single wave of resident CTAs is shared by both (separate launches left the
+// smaller tensor's last wave partly empty).  The scratch is caller-provided workspace
+// (zyfa_hadamard_quantize_e4m3, zyfa_hadamard_quantize_qk_e4m3) or a fixed array inside this
+// library (zyfa_hadamard_quantize_e4m3_noalloc).
 //
 // HBM-bound: per element 2 bytes read twice and 1 byte written.  Each thread rotates whole Hadamard
 // blocks of one row in registers (no cross-lane traffic); a CTA of 128 threads covers 128 rows.  A
@@ -93,6 +97,24 @@ struct Slots {
   static constexpr int kBytes = 2 * kThreads * kPitch;  // two rows per thread: current and next
 };
 
+// The tensors of one launch: blocks [0, np[0]) are tensor 0's, [np[0], np[0] + np[1]) tensor 1's
+// (np[1] = 0 for a single tensor).  A block's partial maximum sits at its global block number.
+struct Pair {
+  const __nv_bfloat16* x[2];
+  uint8_t* x8[2];
+  float* descale[2];
+  long long rows[2];
+  long long np[2];
+};
+
+// Tensor and first row of global block pb (blocks past the end map to tensor 1 beyond its rows,
+// which fetch_rows and the row checks skip).
+__device__ __forceinline__ int block_tensor(const Pair& t, long long pb, long long& r0) {
+  const int k = pb >= t.np[0] ? 1 : 0;
+  r0 = (pb - (k ? t.np[0] : 0)) * 128;
+  return k;
+}
+
 // Start copying the warp's 32 rows [r0, r0 + 32) (those below `rows`) into their threads' slots
 // (slots are kPitch apart from `slots`): each copy instruction moves 32 consecutive 16-byte pieces,
 // 512 contiguous bytes of the tensor.  One commit group per call, empty or not.
@@ -148,26 +170,31 @@ __device__ __forceinline__ float block_max(float m, float* red) {
   return m;
 }
 
-// Pass 1: partial[p] = max |y| over rows [128p, 128p + 128); thread t rotates row 128p + t.
+// Pass 1: partial[p] = max |y| over the rows of global block p; thread t rotates the block's row t.
 template <int D, int N>
-__global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const __nv_bfloat16* __restrict__ x,
-                                                                 long long rows, float* __restrict__ partial,
-                                                                 long long nparts) {
+__global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const __grid_constant__ Pair t,
+                                                                 float* __restrict__ partial) {
   __shared__ float red[kThreads / 32];
   extern __shared__ __align__(16) uint8_t slots_raw[];
   const uint32_t slot0 = static_cast<uint32_t>(__cvta_generic_to_shared(slots_raw)) + threadIdx.x * Slots<D>::kPitch;
   const uint32_t warp_slots = slot0 - (threadIdx.x & 31) * Slots<D>::kPitch;
   const int wrow = threadIdx.x & ~31;                        // the warp's first row in a 128-row block
   constexpr uint32_t kOther = kThreads * Slots<D>::kPitch;  // offset of the second slot
+  const long long nparts = t.np[0] + t.np[1];
   int cur = 0;
-  fetch_rows<D>(x, static_cast<long long>(blockIdx.x) * kRowsPerPartial + wrow, rows, warp_slots);
+  long long r0;
+  int k = block_tensor(t, blockIdx.x, r0);
+  fetch_rows<D>(t.x[k], r0 + wrow, t.rows[k], warp_slots);
   for (long long pb = blockIdx.x; pb < nparts; pb += gridDim.x) {
-    const long long r = pb * kRowsPerPartial + threadIdx.x;
-    fetch_rows<D>(x, (pb + gridDim.x) * kRowsPerPartial + wrow, rows, warp_slots + (cur ^ 1) * kOther);
+    const int kc = block_tensor(t, pb, r0);
+    const long long r = r0 + threadIdx.x;
+    long long rn;
+    const int kn = block_tensor(t, pb + gridDim.x, rn);
+    fetch_rows<D>(t.x[kn], rn + wrow, t.rows[kn], warp_slots + (cur ^ 1) * kOther);
     fetch_wait_prev();
     const uint32_t slot = slot0 + cur * kOther;
     float m = 0.0f;
-    if (r < rows) {
+    if (r < t.rows[kc]) {
 #pragma unroll 1
       for (int c = 0; c < D / N; ++c) {
         float v[N];
@@ -184,30 +211,41 @@ __global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const __nv_bflo
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
-// Pass 2: descale from the partial maxima, then the codes of every row.
+// Pass 2: each tensor's descale from its partial maxima, then the codes of every row.
 template <int D, int N>
-__global__ void __launch_bounds__(kThreads) hadamard_quant_kernel(const __nv_bfloat16* __restrict__ x,
-                                                                  long long rows, const float* __restrict__ partial,
-                                                                  long long nparts, uint8_t* __restrict__ x8,
-                                                                  float* __restrict__ descale_out) {
+__global__ void __launch_bounds__(kThreads) hadamard_quant_kernel(const __grid_constant__ Pair t,
+                                                                  const float* __restrict__ partial) {
   __shared__ float red[kThreads / 32];
-  float m = 0.0f;
-  for (long long i = threadIdx.x; i < nparts; i += kThreads) m = fmaxf(m, partial[i]);
-  const float amax = block_max(m, red);
-  const float ds = amax > 0.0f ? __fdiv_rn(amax, kE4M3Max) : 1.0f;
-  const float sc = amax > 0.0f ? __fdiv_rn(kE4M3Max, amax) : 1.0f;
-  if (blockIdx.x == 0 && threadIdx.x == 0) *descale_out = ds;
+  float sc[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const long long p0 = k ? t.np[0] : 0;
+    float m = 0.0f;
+    for (long long i = threadIdx.x; i < t.np[k]; i += kThreads) m = fmaxf(m, partial[p0 + i]);
+    const float amax = block_max(m, red);
+    const float ds = amax > 0.0f ? __fdiv_rn(amax, kE4M3Max) : 1.0f;
+    sc[k] = amax > 0.0f ? __fdiv_rn(kE4M3Max, amax) : 1.0f;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && t.np[k] > 0) *t.descale[k] = ds;
+  }
   extern __shared__ __align__(16) uint8_t slots_raw[];
   const uint32_t slot0 = static_cast<uint32_t>(__cvta_generic_to_shared(slots_raw)) + threadIdx.x * Slots<D>::kPitch;
   const uint32_t warp_slots = slot0 - (threadIdx.x & 31) * Slots<D>::kPitch;
   const int wrow = threadIdx.x & ~31;
   constexpr uint32_t kOther = kThreads * Slots<D>::kPitch;
+  const long long nparts = t.np[0] + t.np[1];
   int cur = 0;
-  fetch_rows<D>(x, static_cast<long long>(blockIdx.x) * kRowsPerPartial + wrow, rows, warp_slots);
+  long long r0;
+  int k = block_tensor(t, blockIdx.x, r0);
+  fetch_rows<D>(t.x[k], r0 + wrow, t.rows[k], warp_slots);
   for (long long pb = blockIdx.x; pb < nparts; pb += gridDim.x, cur ^= 1) {
-    const long long r = pb * kRowsPerPartial + threadIdx.x;
+    const int kc = block_tensor(t, pb, r0);
+    const long long r = r0 + threadIdx.x;
+    const long long rows = t.rows[kc];
+    const float scale = kc ? sc[1] : sc[0];
     __syncwarp();  // every lane has read the slots the next copies overwrite
-    fetch_rows<D>(x, (pb + gridDim.x) * kRowsPerPartial + wrow, rows, warp_slots + (cur ^ 1) * kOther);
+    long long rn;
+    const int kn = block_tensor(t, pb + gridDim.x, rn);
+    fetch_rows<D>(t.x[kn], rn + wrow, t.rows[kn], warp_slots + (cur ^ 1) * kOther);
     fetch_wait_prev();
     const uint32_t slot = slot0 + cur * kOther;
     if (r < rows) {
@@ -222,10 +260,10 @@ __global__ void __launch_bounds__(kThreads) hadamard_quant_kernel(const __nv_bfl
         for (int i = 0; i < N / 16; ++i) {
           uint32_t w[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float* e = v + 16 * i + 4 * k;
-            w[k] = cvt_e4m3x2(__fmul_rn(e[1], sc), __fmul_rn(e[0], sc)) |
-                   (cvt_e4m3x2(__fmul_rn(e[3], sc), __fmul_rn(e[2], sc)) << 16);
+          for (int q = 0; q < 4; ++q) {
+            const float* e = v + 16 * i + 4 * q;
+            w[q] = cvt_e4m3x2(__fmul_rn(e[1], scale), __fmul_rn(e[0], scale)) |
+                   (cvt_e4m3x2(__fmul_rn(e[3], scale), __fmul_rn(e[2], scale)) << 16);
           }
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + c * N + 16 * i), "r"(w[0]),
                        "r"(w[1]), "r"(w[2]), "r"(w[3])
@@ -238,13 +276,13 @@ __global__ void __launch_bounds__(kThreads) hadamard_quant_kernel(const __nv_bfl
     {
       constexpr int kPieces = D / 16;  // 16-byte pieces of codes per row
       const int lane = threadIdx.x & 31;
-      const long long r0 = pb * kRowsPerPartial + wrow;
-      uint8_t* base = x8 + r0 * D;
+      const long long w0 = r0 + wrow;
+      uint8_t* base = t.x8[kc] + w0 * D;
 #pragma unroll
       for (int i = 0; i < kPieces; ++i) {
         const int q = i * 32 + lane;
         const int row = q / kPieces, piece = q % kPieces;
-        if (r0 + row < rows) {
+        if (w0 + row < rows) {
           uint4 w;
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
@@ -294,9 +332,8 @@ int sm_count() {
 long long num_partials(long long rows) { return (rows + kRowsPerPartial - 1) / kRowsPerPartial; }
 
 template <int D, int N>
-zyfa_status_t launch_both(const void* x, void* x8, float* descale, long long rows, float* partial,
-                          cudaStream_t stream) {
-  const long long np = num_partials(rows);
+zyfa_status_t launch_both(const Pair& t, float* partial, cudaStream_t stream) {
+  const long long np = t.np[0] + t.np[1];
   const int nsm = sm_count();
   if (nsm <= 0) return ZYFA_ERR_CUDA;
   constexpr int kSmem = Slots<D>::kBytes;
@@ -311,10 +348,9 @@ zyfa_status_t launch_both(const void* x, void* x8, float* descale, long long row
     per_sm = 1;
   const long long cap = static_cast<long long>(per_sm) * nsm;
   const int grid = static_cast<int>(np < cap ? np : cap);
-  const auto* xb = static_cast<const __nv_bfloat16*>(x);
-  k1<<<grid, kThreads, kSmem, stream>>>(xb, rows, partial, np);
+  k1<<<grid, kThreads, kSmem, stream>>>(t, partial);
   if (cudaGetLastError() != cudaSuccess) return ZYFA_ERR_CUDA;
-  k2<<<grid, kThreads, kSmem, stream>>>(xb, rows, partial, np, static_cast<uint8_t*>(x8), descale);
+  k2<<<grid, kThreads, kSmem, stream>>>(t, partial);
   return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
@@ -331,11 +367,20 @@ zyfa_status_t check_args(const void* x, const void* x8, const float* descale, lo
   return ZYFA_OK;
 }
 
-zyfa_status_t dispatch(const void* x, void* x8, float* descale, long long rows, int D, float* partial,
-                       cudaStream_t stream) {
-  if (D == 128) return launch_both<128, 128>(x, x8, descale, rows, partial, stream);
-  if (D == 64) return launch_both<64, 64>(x, x8, descale, rows, partial, stream);
-  return launch_both<192, 64>(x, x8, descale, rows, partial, stream);
+zyfa_status_t dispatch(const Pair& t, int D, float* partial, cudaStream_t stream) {
+  if (D == 128) return launch_both<128, 128>(t, partial, stream);
+  if (D == 64) return launch_both<64, 64>(t, partial, stream);
+  return launch_both<192, 64>(t, partial, stream);
+}
+
+Pair make_pair(const void* x, void* x8, float* descale, long long rows) {
+  Pair t = {};
+  t.x[0] = t.x[1] = static_cast<const __nv_bfloat16*>(x);
+  t.x8[0] = t.x8[1] = static_cast<uint8_t*>(x8);
+  t.descale[0] = t.descale[1] = descale;
+  t.rows[0] = rows;
+  t.np[0] = num_partials(rows);
+  return t;
 }
 
 }  // namespace
@@ -352,7 +397,29 @@ zyfa_status_t zyfa_hadamard_quantize_e4m3(const void* x, void* x8, float* descal
   if (st != ZYFA_OK || rows == 0) return st;
   if (!workspace || workspace_bytes < zyfa_hadamard_workspace_bytes(rows)) return ZYFA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 3u) return ZYFA_ERR_MISALIGNED;
-  return dispatch(x, x8, descale, rows, D, static_cast<float*>(workspace), stream);
+  return dispatch(make_pair(x, x8, descale, rows), D, static_cast<float*>(workspace), stream);
+}
+
+// Q and K in one launch per pass: the partial maxima of K follow those of Q in the workspace.
+zyfa_status_t zyfa_hadamard_quantize_qk_e4m3(const void* q, void* q8, float* q_descale, long long q_rows,
+                                             const void* k, void* k8, float* k_descale, long long k_rows, int D,
+                                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  zyfa_status_t st = check_args(q, q8, q_descale, q_rows, D);
+  if (st == ZYFA_OK) st = check_args(k, k8, k_descale, k_rows, D);
+  if (st != ZYFA_OK) return st;
+  if (q_rows == 0 && k_rows == 0) return ZYFA_OK;
+  if (q_rows == 0) return zyfa_hadamard_quantize_e4m3(k, k8, k_descale, k_rows, D, workspace, workspace_bytes, stream);
+  if (k_rows == 0) return zyfa_hadamard_quantize_e4m3(q, q8, q_descale, q_rows, D, workspace, workspace_bytes, stream);
+  if (!workspace || workspace_bytes < zyfa_hadamard_workspace_bytes(q_rows) + zyfa_hadamard_workspace_bytes(k_rows))
+    return ZYFA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 3u) return ZYFA_ERR_MISALIGNED;
+  Pair t = make_pair(q, q8, q_descale, q_rows);
+  t.x[1] = static_cast<const __nv_bfloat16*>(k);
+  t.x8[1] = static_cast<uint8_t*>(k8);
+  t.descale[1] = k_descale;
+  t.rows[1] = k_rows;
+  t.np[1] = num_partials(k_rows);
+  return dispatch(t, D, static_cast<float*>(workspace), stream);
 }
 
 // The allocation-free variant: the same two kernels, with the partial maxima in the library's own
@@ -365,7 +432,7 @@ zyfa_status_t zyfa_hadamard_quantize_e4m3_noalloc(const void* x, void* x8, float
   if (rows > kNoAllocMaxRows) return ZYFA_ERR_UNSUPPORTED;
   float* scratch = noalloc_scratch();
   if (!scratch) return ZYFA_ERR_CUDA;
-  return dispatch(x, x8, descale, rows, D, scratch, stream);
+  return dispatch(make_pair(x, x8, descale, rows), D, scratch, stream);
 }
 
 }  // extern "C"

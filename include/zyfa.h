@@ -27,6 +27,12 @@
  * row's reference contributes at most 2^-127 of its weight (its E8M0 scale is clamped).  FP8 scaled
  * scores (softmax_scale * descales * q.k) must stay below 2^16 binades in magnitude, where the
  * Lean-P offset 55.625 - 8e is still exact in fp32 (attention scores are many orders smaller).
+ *
+ * Per-device state: the library keeps, per device and for the life of the process, the device address
+ * of its status word and of the allocation-free scratch, the shared-memory opt-in of each kernel and
+ * two copy streams for the host-buffer entry point.  Do not use it across cudaDeviceReset() (or any
+ * other teardown of a device's primary context) in the same process: those cached addresses,
+ * attributes and streams would belong to the destroyed context.
  */
 #ifndef ZYFA_H_
 #define ZYFA_H_
@@ -164,6 +170,25 @@ zyfa_status_t zyfa_attn_fwd_causal_host(const void* q_host, const void* k_host, 
  */
 zyfa_status_t zyfa_hadamard_quantize_e4m3(const void* x, void* x8, float* descale, long long rows, int D,
                                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * zyfa_hadamard_quantize_qk_e4m3 - zyfa_hadamard_quantize_e4m3 for Q and K together (same passage):
+ * the same rotation and quantisation, each tensor with its own per-tensor descale, in one launch per
+ * pass instead of two.  Q's and K's 128-row blocks share one wave of CTAs, so the smaller tensor no
+ * longer runs a partly empty wave of its own.
+ *
+ *   q, q8, q_descale, q_rows   Q's input, codes, descale and rows, as x, x8, descale, rows above.
+ *   k, k8, k_descale, k_rows   the same for K.
+ *   D                          the common head dimension, 64, 128 or 192.
+ *   workspace                  at least zyfa_hadamard_workspace_bytes(q_rows) +
+ *                              zyfa_hadamard_workspace_bytes(k_rows) bytes, 4-byte aligned.
+ * Codes and descales equal those of two zyfa_hadamard_quantize_e4m3 calls, bit for bit.  Two kernel
+ * launches on `stream`, asynchronous, allocates nothing; errors as zyfa_hadamard_quantize_e4m3 (either
+ * tensor's).  If one of the two has no rows, only the other is processed.
+ */
+zyfa_status_t zyfa_hadamard_quantize_qk_e4m3(const void* q, void* q8, float* q_descale, long long q_rows,
+                                             const void* k, void* k8, float* k_descale, long long k_rows, int D,
+                                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * zyfa_hadamard_quantize_e4m3_noalloc - zyfa_hadamard_quantize_e4m3 without a workspace argument, for

@@ -9,7 +9,7 @@ import torch
 
 import oracle as O
 from _gpu_util import FP8_TOL, select
-from fp8_causal_prefill_gb300 import api, flash_attn_func, hadamard_quantize_e4m3
+from fp8_causal_prefill_gb300 import api, flash_attn_func, hadamard_quantize_e4m3, hadamard_quantize_qk_e4m3
 from fp8_causal_prefill_gb300.inputs import CONFIGS, Shape, make_problem, quantize_e4m3
 
 pytestmark = pytest.mark.gpu
@@ -106,3 +106,48 @@ def test_workspace_checks():
     assert st == 1
     assert api.zyfa_hadamard_quantize_e4m3(x.data_ptr(), c.data_ptr(), d.data_ptr(), 0, 128, 0, 0) == 0
     assert api.zyfa_hadamard_quantize_e4m3(x.data_ptr(), c.data_ptr(), d.data_ptr(), 600, 96, ws.data_ptr(), 8) == 2
+
+
+@pytest.mark.parametrize("D", [64, 128, 192])
+@pytest.mark.parametrize("q_rows,k_rows", [(1, 1), (4109, 257), (256, 1000), (70001, 13)])
+def test_q_and_k_in_one_launch_equal_the_oracle(q_rows, k_rows, D):
+    # Q and K share a launch per pass but keep their own maxima: codes and descales equal the
+    # oracle's for each tensor on its own, bit for bit (the K maximum differs from Q's on purpose)
+    rng = np.random.default_rng(q_rows + 3 * k_rows + D)
+    xq = _bf16(rng.standard_normal((q_rows, D)) * 3.0)
+    xk = _bf16(rng.standard_normal((k_rows, D)))
+    q8, dq, k8, dk = hadamard_quantize_qk_e4m3(xq.cuda(), xk.cuda())
+    torch.cuda.synchronize()
+    for codes, ds, xb in ((q8, dq, xq), (k8, dk, xk)):
+        ref_codes, ref_ds = _oracle(xb)
+        assert float(ds.item()) == float(ref_ds)
+        assert np.array_equal(codes.view(torch.uint8).cpu().numpy(), ref_codes)
+
+
+def test_q_and_k_in_one_launch_at_the_bench_size_equal_separate_calls():
+    # the bench workload's Q (1,048,576 rows) and K (262,144 rows): the joint call reproduces two
+    # separate calls bit for bit
+    g = torch.Generator(device="cuda").manual_seed(11)
+    xq = torch.randn((1 << 20, 128), generator=g, device="cuda").to(torch.bfloat16)
+    xk = torch.randn((1 << 18, 128), generator=g, device="cuda").to(torch.bfloat16)
+    q8, dq, k8, dk = hadamard_quantize_qk_e4m3(xq, xk)
+    q8s, dqs = hadamard_quantize_e4m3(xq)
+    k8s, dks = hadamard_quantize_e4m3(xk)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dqs) and torch.equal(dk, dks)
+    assert torch.equal(q8.view(torch.uint8), q8s.view(torch.uint8))
+    assert torch.equal(k8.view(torch.uint8), k8s.view(torch.uint8))
+
+
+def test_q_and_k_workspace_and_empty_tensor_checks():
+    x = torch.zeros((600, 128), dtype=torch.bfloat16, device="cuda")
+    c = torch.empty((600, 128), dtype=torch.uint8, device="cuda")
+    d = torch.empty(2, dtype=torch.float32, device="cuda")
+    one = api.zyfa_hadamard_workspace_bytes(600)
+    ws = torch.empty(2 * one // 4, dtype=torch.float32, device="cuda")
+    args = (x.data_ptr(), c.data_ptr(), d.data_ptr(), 600, x.data_ptr(), c.data_ptr(), d.data_ptr() + 4)
+    assert api.zyfa_hadamard_quantize_qk_e4m3(*args, 600, 128, ws.data_ptr(), 2 * one - 4) == 1  # short workspace
+    assert api.zyfa_hadamard_quantize_qk_e4m3(*args, 600, 96, ws.data_ptr(), 2 * one) == 2       # head dim
+    assert api.zyfa_hadamard_quantize_qk_e4m3(*args, 0, 128, ws.data_ptr(), one) == 0            # K empty
+    torch.cuda.synchronize()
+    assert float(d[0].item()) == 1.0                    # all-zero Q: descale 1

@@ -67,3 +67,26 @@ def test_host_entry_rejects_bad_arguments():
     assert api.zyfa_attn_fwd_causal_host(16, 16, 16, 16, 16, 16, 16, 16, 1, 64, 2, 2, 128, 128, 0.0, 0, 0, 0, 0, -1) == 1
     assert api.zyfa_attn_fwd_causal_host(0, 16, 16, 16, 16, 16, 16, 16, 1, 64, 2, 2, 128, 128, 0.0, 0, 0, 0, 0, 2) == 1
     assert api.zyfa_attn_fwd_causal_host(16, 16, 16, 16, 16, 16, 16, 16, 1, 64, 2, 2, 96, 96, 0.0, 0, 0, 0, 0, 2) == 2
+
+
+def test_host_entry_checks_device_buffers_before_any_copy():
+    # a misaligned or missing device buffer is reported before anything is enqueued: the device
+    # buffers and the host output keep their contents
+    p = make_problem(Shape(1, 300, 2, 1, 128, 128), seed=4, bf16=False)
+    host = [t.contiguous().pin_memory() for t in (p.q8, p.k8, p.v8)]
+    out_h = torch.full((1, 300, 2, 128), 7.0, dtype=torch.bfloat16).pin_memory()
+    dev = [torch.zeros(h.numel() + 16, dtype=torch.uint8, device="cuda") for h in host]
+    out_d = torch.zeros(300 * 2 * 128 + 8, dtype=torch.bfloat16, device="cuda")
+    hp = [h.data_ptr() for h in host] + [out_h.data_ptr()]
+
+    def call(qd, kd, vd, od, scale=0.0):
+        return api.zyfa_attn_fwd_causal_host(*hp, qd, kd, vd, od, 1, 300, 2, 1, 128, 128, scale, api.ZYFA_DTYPE_E4M3,
+                                             0, 0, 0, 4, torch.cuda.current_stream().cuda_stream)
+    ok = [d.data_ptr() for d in dev] + [out_d.data_ptr()]
+    assert call(ok[0] + 8, ok[1], ok[2], ok[3]) == 3          # misaligned q_dev
+    assert call(ok[0], ok[1], ok[2], ok[3] + 2) == 3          # misaligned out_dev
+    assert call(ok[0], 0, ok[2], ok[3]) == 1                  # missing k_dev
+    assert call(ok[0], ok[1], ok[2], ok[3], scale=-1.0) == 1  # bad scale
+    torch.cuda.synchronize()
+    assert all(int(d.count_nonzero()) == 0 for d in dev) and int(out_d.count_nonzero()) == 0
+    assert bool((out_h == 7.0).all())

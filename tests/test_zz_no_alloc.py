@@ -42,7 +42,7 @@ def _no_alloc(x):
     return c, ds
 
 
-@pytest.mark.parametrize("d", [128, 192])
+@pytest.mark.parametrize("d", [64, 128, 192])
 def test_no_alloc_equals_workspace_entry_on_two_calls_in_a_row(d):
     # two allocation-free calls back to back: a large input, then a smaller one with a different
     # maximum, which must not see the partial maxima the first call left in the shared scratch
@@ -52,6 +52,18 @@ def test_no_alloc_equals_workspace_entry_on_two_calls_in_a_row(d):
     for (ref_c, ref_ds), (got_c, got_ds) in zip(refs, gots):
         assert torch.equal(got_ds, ref_ds)
         assert torch.equal(got_c, ref_c)
+
+
+def test_no_alloc_at_its_largest_accepted_size():
+    # 4,194,304 rows fill the library's scratch to its last slot (32,768 partial maxima)
+    rows = 4_194_304
+    g = torch.Generator(device="cuda").manual_seed(5)
+    x = torch.randn((rows, 64), generator=g, device="cuda").to(torch.bfloat16)
+    x[rows - 7, 3] = 300.0               # the tensor's maximum sits in the last 128-row block
+    ref_c, ref_ds = _with_workspace(x)
+    got_c, got_ds = _no_alloc(x)
+    assert torch.equal(got_ds, ref_ds)
+    assert torch.equal(got_c, ref_c)
 
 
 def test_no_alloc_rejects_rows_beyond_its_scratch():
