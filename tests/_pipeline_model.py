@@ -15,7 +15,9 @@ random delays. The model checks, at every step:
 - no K/V slot or Q tile overwritten while an MMA still reads it;
 - no score tile overwritten before its warpgroup copied it out;
 - no P tile overwritten while its PV is pending;
-- every PV reads the P and V tiles it should.
+- every PV reads the P and V tiles it should;
+- no output accumulator overwritten by a unit's first PV before the previous unit's output was read
+  out of it, and no output read out while a PV into it is pending or before its unit's last PV.
 
 Each rule mirrors a statement of the kernel source (zyfa_fwd.cuh).  For example, K and V have
 rings of their own exactly when the ring holds three slots or fewer.  The last PV of a query tile
@@ -68,6 +70,7 @@ def simulate(S, BN, stages, units, seed, wrong_release=False, max_steps=2_000_00
     k_data, v_data, q_data = [None] * stages, [None] * stages, [None, None]
     score = {"owner": None, "read": True}
     p_tile, pv_pending = [None, None], [0, 0]
+    o_state = [{"owner": None, "free": True, "pvs": 0}, {"owner": None, "free": True, "pvs": 0}]
     pipe, loads = [], []
 
     def wait(name, k):
@@ -140,7 +143,7 @@ def simulate(S, BN, stages, units, seed, wrong_release=False, max_steps=2_000_00
                 errors.append(f"PV{t}({j}) of unit {r0} reads V of {v_data[st]}")
             pv_pending[t] += 1
             v_refs[st] += 1
-            pipe.append(("pv", t, st))
+            pipe.append(("pv", t, st, r0, j))
             pipe.append(("commit", f"pv_done{t}"))
             pv0_last = n1 == 0 or (j == n0 - 1 and n1 > n0)
             if wrong_release and j == n0 - 1 and n1 > 0:
@@ -233,6 +236,9 @@ def simulate(S, BN, stages, units, seed, wrong_release=False, max_steps=2_000_00
                 pv_ph += 1
                 if pv_pending[t]:
                     errors.append(f"epilogue of warpgroup {t} with a PV pending")
+                if o_state[t] != {"owner": r0, "free": False, "pvs": nt}:
+                    errors.append(f"warpgroup {t} reads out {o_state[t]} for unit {r0} ({nt} PVs)")
+                o_state[t]["free"] = True
 
     roles = [producer(), v_producer(), mma(), softmax(0), softmax(1)]
     blocked = [None] * len(roles)
@@ -250,7 +256,16 @@ def simulate(S, BN, stages, units, seed, wrong_release=False, max_steps=2_000_00
                 k_refs[st] -= 1
                 q_refs[t] -= 1
             elif op[0] == "pv":
-                _, t, st = op
+                _, t, st, r0, j = op
+                if j == 0:
+                    if not o_state[t]["free"]:
+                        errors.append(f"first PV of tile {t} of unit {r0} overwrites the output of "
+                                      f"{o_state[t]['owner']} before it was read out")
+                    o_state[t] = {"owner": r0, "free": False, "pvs": 1}
+                elif o_state[t]["owner"] != r0:
+                    errors.append(f"PV of tile {t} of unit {r0} accumulates into the output of {o_state[t]['owner']}")
+                else:
+                    o_state[t]["pvs"] += 1
                 pv_pending[t] -= 1
                 v_refs[st] -= 1
             else:
