@@ -624,18 +624,20 @@ def main():
                                                args.host_chunks, sptr)
             if st != 0:
                 raise api.ZyfaError(st, "zyfa_attn_fwd_causal_host")
-        for _ in range(2):
+        for _ in range(3):
             host_step()
         barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n_e2e):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e + 1)]
+        ev[0].record(stream)
+        for i in range(n_e2e):
             host_step()
-        e1.record(stream)
+            ev[i + 1].record(stream)
         barrier()
-        te = slowest_rank_ms(e0.elapsed_time(e1) / n_e2e, world, dev)
+        step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(n_e2e)]
+        te = slowest_rank_ms(ev[0].elapsed_time(ev[-1]) / n_e2e, world, dev)
         e2e = {"value": job_throughput(flops, world, te), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": te,
+               "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
                "steps": n_e2e, "call": "zyfa_attn_fwd_causal_host (pinned host buffers)",
                "chunks": args.host_chunks or 4}
 
