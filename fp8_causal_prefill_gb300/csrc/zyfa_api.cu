@@ -270,9 +270,25 @@ zyfa_status_t zyfa_attn_fwd_causal_host(const void* q_host, const void* k_host, 
   if (!std::isfinite(softmax_scale) || softmax_scale < 0.0f) return ZYFA_ERR_INVALID_ARG;
   const long long nqb = (static_cast<long long>(S) + kUnitRows - 1) / kUnitRows;
   if (nqb * B * H > (1ll << 30) || static_cast<long long>(S) > (1ll << 30)) return ZYFA_ERR_UNSUPPORTED;
-  if (chunks == 0) chunks = 4;
-  if (chunks > nqb) chunks = static_cast<int>(nqb);
-  if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;
+  // chunk boundaries in query blocks: `chunks` equal chunks, or for chunks == 0 the library's plan.
+  // Every row's output waits for its chunk's download, and the last chunk's download follows the last
+  // kernel with nothing left to hide it behind; causal work grows with the row, so the plan ends with
+  // two short chunks of nqb/16 query blocks each (short downloads, kernels still long enough to fill
+  // the GPU) after four equal chunks.  Below 32 query blocks (8K rows) those tails would be a block
+  // or two and the plan is four equal chunks.
+  long long bound[kMaxHostChunks + 1];
+  if (chunks == 0 && nqb >= 32) {
+    const long long tail = (nqb + 8) / 16, body = nqb - 2 * tail;
+    chunks = 6;
+    for (int c = 0; c <= 4; ++c) bound[c] = body * c / 4;
+    bound[5] = body + tail;
+    bound[6] = nqb;
+  } else {
+    if (chunks == 0) chunks = 4;
+    if (chunks > nqb) chunks = static_cast<int>(nqb);
+    if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;
+    for (int c = 0; c <= chunks; ++c) bound[c] = nqb * c / chunks;
+  }
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ZYFA_ERR_CUDA;
   cudaStream_t up = nullptr, down = nullptr;
@@ -293,7 +309,7 @@ zyfa_status_t zyfa_attn_fwd_causal_host(const void* q_host, const void* k_host, 
   bool ok = cudaEventRecord(ev.e[0], stream) == cudaSuccess && cudaStreamWaitEvent(up, ev.e[0], 0) == cudaSuccess;
   zyfa_status_t st = ZYFA_OK;
   for (int c = 0; ok && c < chunks; ++c) {
-    const long long qb0 = nqb * c / chunks, qb1 = nqb * (c + 1) / chunks;
+    const long long qb0 = bound[c], qb1 = bound[c + 1];
     const long long r0 = qb0 * kUnitRows, r1 = std::min<long long>(qb1 * kUnitRows, S);
     ok = copy_rows(q_dev, q_host, row_q, r0, r1, cudaMemcpyHostToDevice, up) &&
          copy_rows(k_dev, k_host, row_k, r0, r1, cudaMemcpyHostToDevice, up) &&

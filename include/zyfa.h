@@ -121,8 +121,11 @@ zyfa_status_t zyfa_attn_fwd_causal_ex(const void* q, const void* k, const void* 
  * zyfa_attn_fwd_causal_host - zyfa_attn_fwd_causal for inputs and output in host memory, with the
  * transfers overlapped with the computation.
  *
- * The query rows are split into `chunks` groups of 256-row blocks (0 = 4; at most 64 and at most one
- * per block).  Chunk c's rows of q, k and v are copied to the device buffers on an internal upload
+ * The query rows are split into `chunks` equal groups of 256-row blocks (at most 64 and at most one per
+ * block).  chunks = 0 selects the library's plan: with 32 blocks or more (S > 7,936), four equal
+ * groups over the first 7/8 of the blocks and two short groups of 1/16 each at the end (the last
+ * group's download cannot overlap any computation, so it is kept short); below that, four equal
+ * groups.  Chunk c's rows of q, k and v are copied to the device buffers on an internal upload
  * stream; the kernel for chunk c's query rows then runs on `stream` (causality: those rows read keys
  * and values of chunks <= c only, all already uploaded); its output rows are copied back on an
  * internal download stream while later chunks compute.  `stream` waits for the last download, so

@@ -47,8 +47,9 @@ def _reference(p, dtype):
 @pytest.mark.parametrize("shape,chunks", [(Shape(1, 1000, 4, 2, 128, 128), 1), (Shape(1, 1000, 4, 2, 128, 128), 3),
                                           (Shape(2, 520, 2, 2, 128, 128), 0), (Shape(1, 8192, 8, 2, 128, 128), 0),
                                           (Shape(1, 700, 2, 2, 192, 128), 64), (Shape(3, 600, 8, 4, 64, 64), 2),
-                                          (Shape(3, 300, 6, 3, 64, 64), 2)],
-                         ids=["S1000c1", "S1000c3", "B2S520", "S8192", "mla-S700-c64", "B3-D64-halves", "B3-D64-oddkv"])
+                                          (Shape(3, 300, 6, 3, 64, 64), 2), (Shape(2, 10000, 4, 2, 128, 128), 0)],
+                         ids=["S1000c1", "S1000c3", "B2S520", "S8192", "mla-S700-c64", "B3-D64-halves", "B3-D64-oddkv",
+                              "B2S10000-tail-plan"])
 def test_host_pipeline_equals_device_call(shape, chunks, dtype):
     p = make_problem(shape, seed=shape.S + chunks)
     out_h, out_d = _run_host(p, dtype, chunks)
