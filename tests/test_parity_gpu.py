@@ -86,8 +86,8 @@ def test_gqa4k_all_rows_four_heads(dtype):
     assert torch.isfinite(out.float()).all()
 
 
-@pytest.mark.parametrize("name,dtype", [("mistral16k", "fp8"), ("bench32k", "fp8"), ("bench32k", "bf16"),
-                                        ("mla32k", "fp8"), ("mla32k", "bf16")])
+@pytest.mark.parametrize("name,dtype", [("mistral16k", "fp8"), ("mistral16k", "bf16"), ("bench32k", "fp8"),
+                                        ("bench32k", "bf16"), ("mla32k", "fp8"), ("mla32k", "bf16")])
 def test_full_size_sampled_rows(name, dtype):
     p = make_problem(CONFIGS[name], seed=0, bf16=(dtype == "bf16"), fp8=(dtype == "fp8"))
     out = run_gpu(p, dtype)
