@@ -11,7 +11,8 @@ The tensor pipe executes issued MMAs and commits in order, at random times. TMA 
 random delays. The model checks, at every step:
 
 - no deadlock;
-- no phase aliasing (a parity wait that could confuse two phases);
+- no phase aliasing: a parity wait is answered the way the hardware answers it, and an answer that
+  differs from the intended one (the phase two ahead, or the phase before) is reported;
 - no K/V slot or Q tile overwritten while an MMA still reads it;
 - no score tile overwritten before its warpgroup copied it out;
 - no P tile overwritten while its PV is pending;
@@ -74,12 +75,16 @@ def simulate(S, BN, stages, units, seed, wrong_release=False, max_steps=2_000_00
     pipe, loads = [], []
 
     def wait(name, k):
+        # answered as the hardware answers a parity wait: complete when the barrier's completed-phase
+        # count has the other parity; any answer that differs from "phase k has completed" is aliasing
         b = bars[name]
 
         def ready():
-            if b.done >= k + 2:
+            hw = (b.done % 2) != (k % 2)
+            if hw != (b.done >= k + 1):
                 errors.append(f"phase aliasing on {name}: {b.done} phases done, waiting for phase {k}")
-            return b.done >= k + 1
+                return True
+            return hw
         return ready
 
     def producer():
