@@ -31,6 +31,10 @@ METRIC = "causal FP8 prefill attention TFLOP/s at S=32K D=128 and % of GB300 FP8
 # Nominal dense tensor peaks (PFLOP/s) used only for the FP8:BF16 ratio applied to the measured bf16 peak.
 NOMINAL_RATIO_FP8_TO_BF16 = 4.5 / 2.25
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# Dense tcgen05 MMA rate per SM and cycle of this GPU, as `bench.py --mma-rate` measures it (clock64
+# spans of back-to-back M=128, N=256 products): the kernel's fraction of the tensor core's own rate at
+# the clock sampled during the timed region.
+MMA_FLOP_PER_CYCLE_PER_SM = {"fp8": 16384, "bf16": 8192}
 
 
 def parse():
@@ -693,6 +697,10 @@ def main():
         if clocks is not None and clocks.get("sm_mhz"):
             # step time x median SM clock: the step in thousands of SM cycles, comparable across clocks
             clocks["kcycles_per_step"] = ms_per_step * clocks["sm_mhz"]
+            nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+            hw = MMA_FLOP_PER_CYCLE_PER_SM[args.dtype] * nsm * clocks["sm_mhz"] * 1e6 / 1e12
+            line["roofline"]["tensor_rate_at_clock"] = hw
+            line["roofline"]["frac_of_tensor_rate"] = achieved / hw
         if e2e is not None:
             line["e2e"] = e2e
         if prepass is not None:
