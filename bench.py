@@ -451,6 +451,26 @@ def run_mma_rate(args):
         fpc = res["burst_flop_per_cycle_per_sm"]
         res["tflops_at_2070_mhz"] = fpc * nsm * 2070e6 / 1e12
         line[name] = res
+    # the attention kernel's own MMA forms, each alone (zyfa_probe_mma_form_rate): FLOP per cycle per SM
+    # from the CTAs' clock64 spans, as a fraction of the dense rate of its type measured above
+    forms = {}
+    names = ("fp8_score_ss_n128", "fp8_pv_block_scaled_ts_n144", "fp8_score_then_pv", "fp8_score_two_n64_halves",
+             "bf16_score_ss_n128", "bf16_score_ss_n64_d192")
+    for form, fname in enumerate(names):
+        fpi = lib.zyfa_probe_mma_form_flops_per_iter(form)
+        iters = 5000
+        cycles = torch.zeros(nsm, dtype=torch.int64, device=dev)
+        flag = torch.zeros(1, dtype=torch.int32, device=dev)
+        for _ in range(3):
+            st = lib.zyfa_probe_mma_form_rate(form, iters, nsm, cycles.data_ptr(), flag.data_ptr(), sptr)
+            if st != 0:
+                raise api.ZyfaError(st, "zyfa_probe_mma_form_rate")
+        torch.cuda.synchronize(dev)
+        fpc = fpi * iters / int(cycles.max().item())
+        dense = line["bf16" if fname.startswith("bf16") else "fp8_e4m3"]["burst_flop_per_cycle_per_sm"]
+        forms[fname] = {"flop_per_cycle_per_sm": fpc, "frac_of_dense": fpc / dense,
+                        "timed_out": int(flag.item()) != 0}
+    line["kernel_mma_forms"] = forms
     print(json.dumps(line), flush=True)
     return 0
 

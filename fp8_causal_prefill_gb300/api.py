@@ -26,7 +26,7 @@ EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_attn_fwd_causal_ex", "zyfa_attn_fwd_ca
             "zyfa_kernel_launches", "zyfa_selftest_stalled_pipeline", "zyfa_hadamard_quantize_e4m3",
             "zyfa_hadamard_quantize_e4m3_noalloc", "zyfa_hadamard_quantize_qk_e4m3", "zyfa_hadamard_workspace_bytes",
             "zyfa_probe_mma_rate",
-            "zyfa_probe_mma_flops_per_iter")
+            "zyfa_probe_mma_flops_per_iter", "zyfa_probe_mma_form_rate", "zyfa_probe_mma_form_flops_per_iter")
 ZYFA_P_LEAN = 0
 ZYFA_P_EXACT = 1
 
@@ -85,6 +85,10 @@ def load_library() -> ctypes.CDLL:
         lib.zyfa_probe_mma_rate.restype = ci
         lib.zyfa_probe_mma_flops_per_iter.argtypes = [ci]
         lib.zyfa_probe_mma_flops_per_iter.restype = ll
+        lib.zyfa_probe_mma_form_rate.argtypes = [ci, ci, ci, vp, vp, vp]
+        lib.zyfa_probe_mma_form_rate.restype = ci
+        lib.zyfa_probe_mma_form_flops_per_iter.argtypes = [ci]
+        lib.zyfa_probe_mma_form_flops_per_iter.restype = ll
         _lib = lib
         return lib
 

@@ -271,6 +271,30 @@ zyfa_status_t zyfa_probe_mma_rate(int fp8, int iters, int grid, long long* cycle
 /* zyfa_probe_mma_flops_per_iter - floating-point operations of one probe iteration per CTA. */
 long long zyfa_probe_mma_flops_per_iter(int fp8);
 
+/*
+ * zyfa_probe_mma_form_rate - the tensor-core rate of one of the attention kernel's own MMA forms,
+ * issued back to back with nothing else in the loop: what each kind of product in the kernel reaches
+ * by itself, against which the kernel's schedule is judged.
+ *
+ *   form       0  FP8 score tile: M=128, N=128, D=128, both operands in shared memory;
+ *              1  FP8 PV: block-scaled (e8m0 factors in tensor memory), M=128, N=144 (D_v = 128 plus the
+ *                 16 row-sum columns), 128 keys, P in tensor memory, V in shared memory;
+ *              2  form 0 followed by form 1;
+ *              3  the FP8 score tile as two N=64 halves;
+ *              4  BF16 score tile: M=128, N=128, D=128;
+ *              5  BF16 score tile of the MLA shape: M=128, N=64, D=192.
+ *   iters, grid, cycles, timed_out, stream: as for zyfa_probe_mma_rate; one iteration is
+ *              zyfa_probe_mma_form_flops_per_iter(form) floating-point operations per CTA.
+ * Returns ZYFA_ERR_INVALID_ARG for bad arguments, ZYFA_ERR_CUDA if the launch fails.  This call has
+ * no counterpart in the pages: it is measurement support.
+ */
+zyfa_status_t zyfa_probe_mma_form_rate(int form, int iters, int grid, long long* cycles, int* timed_out,
+                                       cudaStream_t stream);
+
+/* zyfa_probe_mma_form_flops_per_iter - floating-point operations of one iteration of `form` (-1 if
+ * the form is unknown). */
+long long zyfa_probe_mma_form_flops_per_iter(int form);
+
 #ifdef __cplusplus
 }
 #endif
