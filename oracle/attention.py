@@ -40,7 +40,17 @@ may be evaluated; the row loop is chunked only to bound memory and does not chan
   exponential per probability, the vector work Lean P removes).  Block exponents and the rounded-sum
   normalisation are those of O2.
 
-* Log-sum-exp (``return_lse=True`` on O1, O2, O2x and O4): ``lse_i = ln sum_j exp(s_ij)`` with
+* ``exactp_noblock_causal_attention`` (O2xn): O2x without the per-block scaling, the ablation of
+  technique (2): every probability is rounded against the row's reference exponent instead of its
+  block's, ``code = rne_e4m3(2^fl32(S32*a/8 - m))``.  A one-pass attention knows only the reference
+  of the keys seen so far, so ``m`` is a running reference (reading): keys go in tiles of 128 from key
+  0; ``m`` is the first tile's largest block exponent and is raised to a later tile's largest block
+  exponent when that exceeds it by more than 8 binades; a tile's codes use the reference after that
+  tile's update, and earlier weights are rescaled by the exact power of two ``2^(m_tile - m_last)``.
+  Probabilities more than about 9 binades below the reference round to zero (the e4m3 subnormal
+  floor), which is what the block scaling avoids.  Normalisation by the rounded sum, as O2.
+
+* Log-sum-exp (``return_lse=True`` on O1, O2, O2x, O2xn and O4): ``lse_i = ln sum_j exp(s_ij)`` with
   ``s_ij`` the real (descaled) score.  For O1 it is computed in float64 from the exact scores; for the
   block-scaled paths it is ``ln sum_j dec(code_ij) 2^e_b`` (the rounded weights carry the
   probabilities' scale), for O4 ``ln sum_j p_j + M ln 2``.  flash_attn_func returns the same
@@ -67,6 +77,8 @@ from .formats import e4m3_decode, e4m3_encode_rne_satfinite, fl32
 
 LEANP_C0 = 55.625
 SCALE_BLOCK = 64
+ONLINE_TILE = 128       # O2xn: keys per step of the running reference
+RESCALE_BINADES = 8     # O2xn: the running reference rises when a tile exceeds it by more than this
 LOG2E = math.log2(math.e)
 LOG2E_F32 = float(np.float32(LOG2E))
 LOG2E_X8_F32 = float(np.float32(8.0 * LOG2E))
@@ -151,6 +163,42 @@ def _leanp_weights(s32, valid, a, c0, block, exact=False):
     w = e4m3_decode(code.astype(np.uint8)) * np.exp2(np.where(valid, rel, 0.0))
     w = np.where(valid & (rel >= -126), w, 0.0)
     return code, e, w
+
+
+def exactp_noblock_weights(s32, valid, a, tile: int = ONLINE_TILE, threshold: int = RESCALE_BINADES,
+                           block: int = SCALE_BLOCK):
+    """O2xn weights of a set of rows: exact P against the row's running reference exponent.
+
+    ``s32`` [R, N] raw fp32 scores (as float64), ``valid`` [R, N] visibility.  Keys are taken in
+    tiles of ``tile`` from key 0.  Per row and tile with a visible key: the block exponents
+    ``ceil(max fl32(S32*a) / 8)`` of its 64-key blocks (visible keys only) and their maximum
+    ``e_top``; the reference ``m`` starts at the first such tile's ``e_top`` and becomes ``e_top``
+    whenever ``e_top > m + threshold``.  The tile's codes are ``rne_e4m3(2^fl32(S32*a/8 - m))``.
+    Returns (codes [R,N], m_last [R], w [R,N]) with ``w = dec(code) * 2^(m_tile - m_last)``."""
+    s32 = np.atleast_2d(np.asarray(s32, dtype=np.float64))
+    valid = np.broadcast_to(np.asarray(valid, dtype=bool), s32.shape)
+    r, n = s32.shape
+    u = np.where(valid, fl32(s32 * a), -np.inf)
+    code = np.zeros((r, n), dtype=np.int64)
+    m_key = np.zeros((r, n))
+    m = np.full(r, np.nan)
+    for t0 in range(0, n, tile):
+        t1 = min(t0 + tile, n)
+        e_top = np.full(r, -np.inf)
+        for b0 in range(t0, t1, block):
+            with np.errstate(invalid="ignore"):
+                e_top = np.maximum(e_top, np.ceil(u[:, b0:min(b0 + block, t1)].max(axis=1) * 0.125))
+        seen = np.isfinite(e_top)                        # rows with a visible key in this tile
+        raise_ = seen & (np.isnan(m) | (e_top > m + threshold))
+        m = np.where(raise_, e_top, m)
+        m_tile = np.where(seen, m, 0.0)[:, None]
+        vis = valid[:, t0:t1]
+        c = exactp_code(np.where(vis, s32[:, t0:t1] * (a / 8.0) - m_tile, -np.inf))
+        code[:, t0:t1] = np.where(vis, c, 0)
+        m_key[:, t0:t1] = m_tile
+    m_last = np.where(np.isnan(m), 0.0, m)
+    w = np.where(valid, e4m3_decode(code.astype(np.uint8)) * np.exp2(m_key - m_last[:, None]), 0.0)
+    return code, m_last, w
 
 
 def _heads(h_total, heads):
@@ -242,6 +290,33 @@ def exactp_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=None, he
     """O2x: O2 with exact exponentiation and rounding of each probability in place of Lean P."""
     return leanp_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=rows, heads=heads,
                                   return_lse=return_lse, exact=True)
+
+
+def exactp_noblock_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=None, heads=None,
+                                    return_lse: bool = False):
+    """O2xn: O2x without the per-block scaling (each probability rounded against the row's running
+    reference exponent), normalised by the rounded sum."""
+    a = fp8_score_scale(softmax_scale, dq, dk)
+    b_, s_, h_, _ = q8.shape
+    hkv, dvd = k8.shape[2], v8.shape[3]
+    rows = _rows(s_, rows)
+    hs = _heads(h_, heads)
+    out = np.zeros((b_, len(rows), len(hs), dvd))
+    lse = np.zeros((b_, len(rows), len(hs)))
+    n_keys = int(rows.max()) + 1 if len(rows) else 0
+    for b in range(b_):
+        for oi, h in enumerate(hs):
+            kh = h // (h_ // hkv)
+            kk, vv = e4m3_decode(k8[b, :n_keys, kh, :]), e4m3_decode(v8[b, :n_keys, kh, :])
+            qh = e4m3_decode(q8[b, :, h, :])
+            for c in range(0, len(rows), _ROW_CHUNK):
+                ri = rows[c:c + _ROW_CHUNK]
+                n = int(ri.max()) + 1 if len(ri) else 0
+                s32 = fl32(qh[ri] @ kk[:n].T)
+                _, m_last, w = exactp_noblock_weights(s32, _causal_mask(ri, n), a)
+                out[b, c:c + len(ri), oi, :] = float(dv) * (w @ vv[:n]) / w.sum(axis=1, keepdims=True)
+                lse[b, c:c + len(ri), oi] = np.log(w.sum(axis=1)) + m_last * math.log(2.0)
+    return (out, lse) if return_lse else out
 
 
 def plain_fp8_causal_attention(q8, k8, v8, dq, dk, dv, softmax_scale, rows=None, heads=None):

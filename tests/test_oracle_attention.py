@@ -219,7 +219,7 @@ def test_zero_queries_give_prefix_mean_on_every_path():
     v8 = O.e4m3_encode_rne_satfinite(vvals)
     dv = 0.25
     mean = np.cumsum(vvals[0, :, 0, :], axis=0) / np.arange(1, s + 1)[:, None] * dv
-    for f in (O.leanp_causal_attention, O.plain_fp8_causal_attention):
+    for f in (O.leanp_causal_attention, O.plain_fp8_causal_attention, O.exactp_noblock_causal_attention):
         out = f(q8, k8, v8, 0.5, 0.5, dv, 0.125)
         for hh in range(2):
             np.testing.assert_allclose(out[0, :, hh, :], mean, rtol=1e-14, atol=1e-15)
@@ -391,7 +391,7 @@ def test_lse_of_zero_queries_is_log_of_row_length_on_every_path():
     k8 = O.e4m3_encode_rne_satfinite(rng.standard_normal((1, s, 1, 16)))
     v8 = O.e4m3_encode_rne_satfinite(rng.standard_normal((1, s, 1, 8)))
     expect = np.log(np.arange(1, s + 1))[None, :, None]
-    for f in (O.leanp_causal_attention, O.exactp_causal_attention):
+    for f in (O.leanp_causal_attention, O.exactp_causal_attention, O.exactp_noblock_causal_attention):
         _, lse = f(q8, k8, v8, 0.5, 0.5, 1.0, 0.125, return_lse=True)
         np.testing.assert_allclose(lse, np.repeat(expect, 2, axis=2), rtol=0, atol=1e-13)
     _, lse1 = O.exact_causal_attention(np.zeros((1, s, 2, 16)), O.e4m3_decode(k8), O.e4m3_decode(v8), 0.125,
@@ -471,3 +471,87 @@ def test_leanp_weight_is_dropped_beyond_the_e8m0_range():
         assert list(e[0]) == [0.0, -float(below)]
         assert np.all(code == 56) and np.all(w[0, :64] == 1.0)
         assert np.all(w[0, 64:] == expect), (below, w[0, 64])
+
+
+# ----------------------------------------------------------------------------------------------
+# O2xn: exact P without the per-block scaling (the ablation of the per-64-key power-of-two scaling)
+
+
+def test_noblock_equals_block_scaled_when_every_block_shares_the_reference():
+    # With a = 8 the exponent argument is the score itself.  Scores in (2, 3] with each 64-key block
+    # reaching above 2.9: every block exponent is 3, the running reference is 3 from the first tile
+    # on, so rounding against the reference is rounding against the block: O2xn == O2x, code for code.
+    rng = np.random.default_rng(21)
+    s32 = rng.uniform(2.01, 2.99, size=(3, 320))
+    s32[:, ::64] = 2.995
+    valid = np.ones(s32.shape, dtype=bool)
+    c_blk, _, w_blk = O.attention._leanp_weights(s32, valid, 8.0, O.LEANP_C0, 64, exact=True)
+    c_nb, m_last, w_nb = O.exactp_noblock_weights(s32, valid, 8.0)
+    assert np.array_equal(m_last, np.full(3, 3.0))
+    assert np.array_equal(c_nb, c_blk)
+    assert np.array_equal(w_nb, w_blk)
+
+
+def test_noblock_rounds_far_blocks_to_zero_where_block_scaling_keeps_them():
+    # One tile: block 0 scores near 0.5 (exponent 1), block 1 scores near -11.5 (exponent -11).  Against
+    # the row reference 1, 2^-12.5 lies below half the smallest e4m3 subnormal (2^-10): every code of
+    # block 1 is 0, while the block-scaled path rounds 2^-0.5 and keeps weight 2^-12 per key.
+    s32 = np.concatenate([np.full((1, 64), 0.5), np.full((1, 64), -11.5)], axis=1)
+    valid = np.ones(s32.shape, dtype=bool)
+    c_nb, _, w_nb = O.exactp_noblock_weights(s32, valid, 8.0)
+    assert np.all(c_nb[0, 64:] == 0) and np.all(w_nb[0, 64:] == 0.0)
+    _, _, w_blk = O.attention._leanp_weights(s32, valid, 8.0, O.LEANP_C0, 64, exact=True)
+    # 2^-0.5 = 0.7071 rounds to the e4m3 value 0.6875; the block scale 2^(-11 - 1) keeps it
+    np.testing.assert_array_equal(w_blk[0, 64:], np.full(64, 0.6875 * 2.0 ** -12))
+    # and the output with V = 0 on block 0, 1 on block 1: 0 without block scaling, > 0 with it
+    v = np.concatenate([np.zeros(64), np.ones(64)])
+    assert (w_nb @ v)[0] == 0.0 and (w_blk @ v)[0] > 0.0
+
+
+def test_noblock_running_reference_rises_only_beyond_eight_binades():
+    # Keys 0 and 128 visible with scores t0 = 0.3 and t1; every other key far below.  Tile 0's
+    # reference is ceil(0.3) = 1.
+    def weights(t1):
+        s32 = np.full((1, 256), -1000.0)
+        s32[0, 0], s32[0, 128] = 0.3, t1
+        return O.exactp_noblock_weights(s32, np.ones(s32.shape, dtype=bool), 8.0)
+
+    # t1 = 8.5: exponent 9 = 1 + 8 is not above the threshold, the reference stays 1:
+    # w1 = e4m3(2^7.5 = 181.02) = 176, w0 = e4m3(2^-0.7 = 0.6156) = 0.625
+    c, m_last, w = weights(8.5)
+    assert m_last[0] == 1.0
+    assert (w[0, 0], w[0, 128]) == (0.625, 176.0)
+    # t1 = 9.5: exponent 10 > 9, the reference becomes 10 for tile 1; tile 0's code keeps its rounding
+    # against 1 and its weight is rescaled exactly: w0 = 0.625 * 2^-9, w1 = e4m3(2^-0.5) = 0.6875
+    c, m_last, w = weights(9.5)
+    assert m_last[0] == 10.0
+    assert (w[0, 0], w[0, 128]) == (0.625 * 2.0 ** -9, 0.6875)
+    # rounding tile 0 against the final reference instead would give 2^-9 (the smallest subnormal)
+    assert O.e4m3_decode(O.exactp_code(np.array([0.3 - 10.0])))[0] == 2.0 ** -9
+
+
+def test_noblock_later_tile_far_below_the_reference_rounds_to_zero():
+    # Tile 0 sets the reference 1 (key 0 at 0.3); tile 1 lies near -11.5, below the reference, which
+    # therefore does not move.  Rounded against the reference, 2^-12.5 is zero; rounded against the
+    # tile's own exponent (-11) it would be e4m3(2^-0.5) = 0.6875 scaled by 2^-12.
+    s32 = np.full((1, 256), -11.5)
+    s32[0, 0] = 0.3
+    s32[0, 1:128] = -1000.0
+    c, m_last, w = O.exactp_noblock_weights(s32, np.ones(s32.shape, dtype=bool), 8.0)
+    assert m_last[0] == 1.0
+    assert w[0, 0] == 0.625
+    assert np.all(c[0, 128:] == 0) and np.all(w[0, 128:] == 0.0)
+
+
+def test_noblock_attention_is_causal_and_close_to_exact_on_gaussian():
+    # Gaussian scores stay within a few binades of the row maximum, where e4m3 rounding against the
+    # reference loses little: O2xn stays near float64 attention, and future keys do not matter.
+    p = make_problem(Shape(1, 300, 2, 1, 64, 32), seed=22, bf16=False)
+    q8, k8, v8 = p.q8.numpy(), p.k8.numpy(), p.v8.numpy()
+    out = O.exactp_noblock_causal_attention(q8, k8, v8, p.dq, p.dk, p.dv, 0.125)
+    ref = O.exact_causal_attention(O.dequant_e4m3(q8, p.dq), O.dequant_e4m3(k8, p.dk), O.dequant_e4m3(v8, p.dv), 0.125)
+    assert O.rel_l2(out, ref) < 0.05
+    k2, v2 = k8.copy(), v8.copy()
+    k2[:, 200:], v2[:, 200:] = 0x38, 0x38
+    out2 = O.exactp_noblock_causal_attention(q8, k2, v2, p.dq, p.dk, p.dv, 0.125)
+    np.testing.assert_array_equal(out2[:, :200], out[:, :200])
