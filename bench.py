@@ -52,8 +52,9 @@ def parse():
     ap.add_argument("--energy-seconds", type=float, default=1.0)
     ap.add_argument("--hadamard", action="store_true",
                     help="also time the Hadamard rotation + quantisation pre-pass of Q and K (bf16 in)")
-    ap.add_argument("--p-mode", choices=["lean", "exact"], default="lean",
-                    help="FP8 probabilities: Lean P (the method) or exact exponential (the ablation)")
+    ap.add_argument("--p-mode", choices=["lean", "exact", "exact-noblock"], default="lean",
+                    help="FP8 probabilities: Lean P (the method), exact exponential (the ablation), or exact "
+                         "without the per-block scaling")
     ap.add_argument("--mma-rate", action="store_true",
                     help="measure the dense FP8 and BF16 tcgen05 MMA rate (burst and sustained) instead")
     ap.add_argument("--no-e2e", action="store_true")
@@ -95,7 +96,8 @@ def shape_for(args):
 
 
 def workload_name(sh, dtype, p_mode="lean"):
-    extra = ", exact-P ablation" if (dtype == "fp8" and p_mode == "exact") else ""
+    extra = {"exact": ", exact-P ablation", "exact-noblock": ", exact-P ablation without block scaling"}.get(
+        p_mode, "") if dtype == "fp8" else ""
     return (f"{'e4m3' if dtype == 'fp8' else 'bf16'} causal prefill B={sh.B} H={sh.H} H_kv={sh.H_kv} S={sh.S} "
             f"D_qk={sh.D_qk} D_v={sh.D_v} {sh.kind} inputs{extra}")
 
@@ -513,7 +515,8 @@ def main():
     sptr = stream.cuda_stream
     api.load_library()
 
-    p_mode = api.ZYFA_P_EXACT if args.p_mode == "exact" else api.ZYFA_P_LEAN
+    p_mode = {"exact": api.ZYFA_P_EXACT, "exact-noblock": api.ZYFA_P_EXACT_NO_BLOCK_SCALE}.get(args.p_mode,
+                                                                                              api.ZYFA_P_LEAN)
 
     def step(q, k, v, o):
         st = api.zyfa_attn_fwd_causal_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), sh.B, sh.S, sh.H,
@@ -702,7 +705,7 @@ def main():
         if os.path.exists(tpath):
             with open(tpath) as f:
                 td = json.load(f)
-            key = f"{args.dtype}:{args.config}" + (":exact" if args.p_mode == "exact" else "")
+            key = f"{args.dtype}:{args.config}" + (f":{args.p_mode}" if args.p_mode != "lean" else "")
             if key in td and not args.heads and not args.seq and td[key].get("kernel_sha256") == kernel_source_hash():
                 traffic = td[key].get("bytes_per_launch")
         line = {

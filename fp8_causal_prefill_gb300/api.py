@@ -29,6 +29,8 @@ EXPORTED = ("zyfa_attn_fwd_causal", "zyfa_attn_fwd_causal_ex", "zyfa_attn_fwd_ca
             "zyfa_probe_mma_flops_per_iter", "zyfa_probe_mma_form_rate", "zyfa_probe_mma_form_flops_per_iter")
 ZYFA_P_LEAN = 0
 ZYFA_P_EXACT = 1
+ZYFA_P_EXACT_NO_BLOCK_SCALE = 2
+_P_MODES = {"lean": ZYFA_P_LEAN, "exact": ZYFA_P_EXACT, "exact-noblock": ZYFA_P_EXACT_NO_BLOCK_SCALE}
 
 
 class FwdOptions(ctypes.Structure):
@@ -162,7 +164,8 @@ def flash_attn_func(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_s
     FP8 inputs are ``torch.float8_e4m3fn`` (or ``torch.uint8`` holding e4m3 bit patterns) with optional
     descales: float32 CUDA tensors of one value (per tensor) or of B*H_kv values ([batch][KV head]); all
     three given descales must use the same form.  BF16 inputs are ``torch.bfloat16``.  ``p_mode`` picks
-    how FP8 probabilities are produced ("lean": Lean P; "exact": exponential and e4m3 rounding).
+    how FP8 probabilities are produced ("lean": Lean P; "exact": exponential and e4m3 rounding;
+    "exact-noblock": the same against the row's running reference, without per-block scaling).
     Returns a bfloat16 tensor [B,S,H,D_v], and with ``return_lse`` also the float32 log-sum-exp
     [B,H,S].  Runs on the current CUDA stream.
     """
@@ -189,8 +192,8 @@ def flash_attn_func(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_s
         out = torch.empty((B, S, H, D_v), dtype=torch.bfloat16, device=q.device)
     elif out.shape != (B, S, H, D_v) or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous bfloat16 [B,S,H,D_v] tensor")
-    if p_mode not in ("lean", "exact"):
-        raise ValueError("p_mode must be 'lean' or 'exact'")
+    if p_mode not in _P_MODES:
+        raise ValueError("p_mode must be 'lean', 'exact' or 'exact-noblock'")
     descales = [_descale_ptr(t, B * H_kv) for t in (q_descale, k_descale, v_descale)]
     forms = {per for _, per in descales if per is not None}
     if len(forms) > 1:
@@ -201,7 +204,7 @@ def flash_attn_func(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_s
         st = zyfa_attn_fwd_causal_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, H, H_kv, D_qk,
                                      D_v, 0.0 if softmax_scale is None else softmax_scale, dtype,
                                      descales[0][0], descales[1][0], descales[2][0],
-                                     ZYFA_P_EXACT if p_mode == "exact" else ZYFA_P_LEAN,
+                                     _P_MODES[p_mode],
                                      1 if forms == {True} else 0, lse.data_ptr() if lse is not None else 0, stream)
     if st != 0:
         raise ZyfaError(st, "zyfa_attn_fwd_causal_ex")

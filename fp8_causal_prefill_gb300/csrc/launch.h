@@ -24,6 +24,7 @@ struct LaunchArgs {
   int stall_loads;    // nonzero only for the stalled-pipeline self-test
   float* lse;         // optional log-sum-exp output [B,H,S]
   int desc_per_head;  // descales indexed by (batch, KV head)
+  int no_block_scale; // exact P only: round against the row reference, no per-block scaling
   int grid;
   Maps maps;
   cudaStream_t stream;

@@ -172,7 +172,8 @@ zyfa_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, i
   if (dtype != ZYFA_DTYPE_E4M3 && dtype != ZYFA_DTYPE_BF16) return ZYFA_ERR_INVALID_ARG;
   zyfa_fwd_options_t o = {ZYFA_P_LEAN, 0, nullptr};
   if (opts) o = *opts;
-  if (o.p_mode != ZYFA_P_LEAN && o.p_mode != ZYFA_P_EXACT) return ZYFA_ERR_INVALID_ARG;
+  if (o.p_mode != ZYFA_P_LEAN && o.p_mode != ZYFA_P_EXACT && o.p_mode != ZYFA_P_EXACT_NO_BLOCK_SCALE)
+    return ZYFA_ERR_INVALID_ARG;
   if (o.descale_per_kv_head != 0 && o.descale_per_kv_head != 1) return ZYFA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(o.lse) & 3u) != 0) return ZYFA_ERR_MISALIGNED;
   if (!std::isfinite(softmax_scale) || softmax_scale < 0.0f) return ZYFA_ERR_INVALID_ARG;
@@ -216,7 +217,8 @@ zyfa_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, i
   a.stall_loads = stall_loads;
   a.lse = o.lse;
   a.desc_per_head = fp8 ? o.descale_per_kv_head : 0;
-  if (fp8 && o.p_mode == ZYFA_P_EXACT) {
+  a.no_block_scale = fp8 && o.p_mode == ZYFA_P_EXACT_NO_BLOCK_SCALE ? 1 : 0;
+  if (fp8 && (o.p_mode == ZYFA_P_EXACT || o.p_mode == ZYFA_P_EXACT_NO_BLOCK_SCALE)) {
     if (D_qk == 64) return run<true, 64, 64, true>(a, q, k, v);
     if (D_qk == 128) return run<true, 128, 128, true>(a, q, k, v);
     return run<true, 192, 128, true>(a, q, k, v);

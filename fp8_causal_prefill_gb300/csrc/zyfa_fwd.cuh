@@ -148,6 +148,7 @@ struct Params {
   int stall_loads;  // self-test of the timeout path: the producer withholds every load
   float* lse;       // optional [B,H,S] natural-log sum of exp of the scores (nullptr: not written)
   int desc_per_head;  // descales are arrays [B][H_kv] (1) or single values (0)
+  int no_block_scale; // exact P only: every block rounds against the row reference (scale factor 1)
 };
 
 struct __align__(8) SharedCtl {
@@ -818,7 +819,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (FP8) {
 #pragma unroll
           for (int b = 0; b < kNB; ++b) {
-            const int eb = e[b] == kNoExp ? m_ref : e[b];
+            int eb = e[b] == kNoExp ? m_ref : e[b];
+            // the ablation of the block scaling: the row's running reference for every block
+            if constexpr (EXACT) eb = p.no_block_scale ? m_ref : eb;
             if constexpr (EXACT) exactp_block(s + 64 * b, a8, eb, *reinterpret_cast<uint32_t(*)[16]>(pw + 16 * b));
             else leanp_block(s + 64 * b, a24, eb, *reinterpret_cast<uint32_t(*)[16]>(pw + 16 * b));
             int sf = 127 + eb - m_ref;

@@ -88,8 +88,13 @@ zyfa_status_t zyfa_attn_fwd_causal(const void* q, const void* k, const void* v, 
 
 /* How FP8 probabilities are produced (ZYFA abstract, technique (1); captivela ZYFA article, "Tiga Trik"). */
 typedef enum {
-  ZYFA_P_LEAN = 0, /* Lean P: one multiply-add and one rounding per probability (the default)       */
-  ZYFA_P_EXACT = 1 /* exact P: hardware exponential, then e4m3 rounding (the pages' comparison point)  */
+  ZYFA_P_LEAN = 0,  /* Lean P: one multiply-add and one rounding per probability (the default)      */
+  ZYFA_P_EXACT = 1, /* exact P: hardware exponential, then e4m3 rounding (the pages' comparison point) */
+  ZYFA_P_EXACT_NO_BLOCK_SCALE = 2 /* exact P rounded against the row's running reference exponent,
+                       with no per-64-key power-of-two scaling: the ablation of technique (2)
+                       (spbcomputers.ru ZYFA article, "Три приёма").  The reference is the first
+                       128-key tile's largest block exponent, raised to a later tile's when that
+                       exceeds it by more than 8 binades; probabilities far below it round to 0. */
 } zyfa_p_mode_t;
 
 /* Optional behaviour of zyfa_attn_fwd_causal_ex.  A zero-initialised struct (or NULL) gives the

@@ -86,6 +86,10 @@ def test_options_validation(lib):
                                      ct.byref(odd_lse), None)
     assert st == 3
     # S == 0 with valid options returns OK without touching the device
-    ok = api.FwdOptions(1, 1, None)
+    for mode in (api.ZYFA_P_LEAN, api.ZYFA_P_EXACT, api.ZYFA_P_EXACT_NO_BLOCK_SCALE):
+        ok = api.FwdOptions(mode, 1, None)
+        assert lib.zyfa_attn_fwd_causal_ex(16, 16, 16, 16, 1, 0, 2, 2, 128, 128, 0.0, 0, None, None, None,
+                                           ct.byref(ok), None) == 0
+    bad_mode = api.FwdOptions(3, 0, None)
     assert lib.zyfa_attn_fwd_causal_ex(16, 16, 16, 16, 1, 0, 2, 2, 128, 128, 0.0, 0, None, None, None,
-                                       ct.byref(ok), None) == 0
+                                       ct.byref(bad_mode), None) == 1

@@ -28,7 +28,7 @@ def test_sequence_of_128k_tokens_sampled_rows():
     assert torch.isfinite(out.float()).all()
 
 
-@pytest.mark.parametrize("p_mode", ["lean", "exact"])
+@pytest.mark.parametrize("p_mode", ["lean", "exact", "exact-noblock"])
 def test_extreme_score_range(p_mode):
     # the same codes with q/k descales 10x larger: score spreads of ~800 binades per row (up to ~700
     # binades from zero), so many blocks sit more than 127 binades below the row maximum (weight 0 in
@@ -41,7 +41,8 @@ def test_extreme_score_range(p_mode):
     out = flash_attn_func(q, k, v, q_descale=ds[0], k_descale=ds[1], v_descale=ds[2], p_mode=p_mode)
     torch.cuda.synchronize()
     assert zyfa_check_errors() == 0
-    f = O.exactp_causal_attention if p_mode == "exact" else O.leanp_causal_attention
+    f = {"exact": O.exactp_causal_attention, "exact-noblock": O.exactp_noblock_causal_attention}.get(
+        p_mode, O.leanp_causal_attention)
     ref = f(p.q8.numpy(), p.k8.numpy(), p.v8.numpy(), p.dq, p.dk, p.dv, O.default_softmax_scale(128))
     got = select(out)
     assert np.all(np.isfinite(got))

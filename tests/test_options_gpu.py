@@ -23,7 +23,8 @@ def _oracle(p, dtype, p_mode="lean", rows=None, heads=None):
     sc = scale_of(p)
     if dtype == "fp8":
         args = (p.q8.numpy(), p.k8.numpy(), p.v8.numpy(), p.dq, p.dk, p.dv, sc)
-        f = O.exactp_causal_attention if p_mode == "exact" else O.leanp_causal_attention
+        f = {"exact": O.exactp_causal_attention, "exact-noblock": O.exactp_noblock_causal_attention}.get(
+            p_mode, O.leanp_causal_attention)
         return f(*args, rows=rows, heads=heads, return_lse=True)
     g = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
     return O.bf16_causal_attention(g(p.qb), g(p.kb), g(p.vb), sc, rows=rows, heads=heads, return_lse=True)
@@ -47,7 +48,7 @@ def _check_lse(got, ref):
     assert d.max() <= 0.1
 
 
-@pytest.mark.parametrize("p_mode", ["lean", "exact"])
+@pytest.mark.parametrize("p_mode", ["lean", "exact", "exact-noblock"])
 @pytest.mark.parametrize("shape", SHAPES, ids=_id)
 def test_fp8_output_and_lse_match_the_emulation(shape, p_mode):
     p = make_problem(shape, seed=shape.S + 5 * shape.H, bf16=False)
@@ -74,15 +75,16 @@ def test_bf16_lse_matches_the_emulation(shape):
     _check_lse(_lse_select(lse), ref_lse)
 
 
-def test_exact_p_full_size_sampled_rows():
+@pytest.mark.parametrize("p_mode", ["exact", "exact-noblock"])
+def test_exact_p_full_size_sampled_rows(p_mode):
     p = make_problem(CONFIGS["bench32k"], seed=0, bf16=False)
     q, k, v, ds = to_device(p, "fp8")
     out, lse = flash_attn_func(q, k, v, q_descale=ds[0], k_descale=ds[1], v_descale=ds[2], return_lse=True,
-                               p_mode="exact")
+                               p_mode=p_mode)
     torch.cuda.synchronize()
     rows = sample_rows(p.shape.S)
     heads = [0, p.shape.H - 1]
-    ref, ref_lse = _oracle(p, "fp8", "exact", rows=rows, heads=heads)
+    ref, ref_lse = _oracle(p, "fp8", p_mode, rows=rows, heads=heads)
     assert O.rel_l2(select(out, rows=rows, heads=heads), ref) <= FP8_TOL
     _check_lse(_lse_select(lse, rows, heads), ref_lse)
 
@@ -93,6 +95,27 @@ def test_exact_p_differs_from_lean_p():
     a = flash_attn_func(q, k, v, q_descale=ds[0], k_descale=ds[1], v_descale=ds[2])
     b = flash_attn_func(q, k, v, q_descale=ds[0], k_descale=ds[1], v_descale=ds[2], p_mode="exact")
     assert not torch.equal(a, b)
+
+
+def test_exact_p_without_block_scaling_differs_where_blocks_lie_far_below():
+    # the outlier stand-in puts many (row, block) pairs more than 8 binades below the row's reference:
+    # rounding them against the reference changes the output, and each mode matches its own emulation
+    p = make_problem(Shape(1, 1024, 2, 1, 128, 128, "mistral"), seed=4, bf16=False)
+    q, k, v, ds = to_device(p, "fp8")
+    a = flash_attn_func(q, k, v, q_descale=ds[0], k_descale=ds[1], v_descale=ds[2], p_mode="exact")
+    b = flash_attn_func(q, k, v, q_descale=ds[0], k_descale=ds[1], v_descale=ds[2], p_mode="exact-noblock")
+    torch.cuda.synchronize()
+    assert not torch.equal(a, b)
+    for mode, got in (("exact", a), ("exact-noblock", b)):
+        ref, _ = _oracle(p, "fp8", mode)
+        assert O.rel_l2(select(got), ref) <= FP8_TOL
+
+
+def test_unknown_p_mode_is_rejected():
+    p = make_problem(Shape(1, 64, 1, 1, 64, 64), seed=1, bf16=False)
+    q, k, v, ds = to_device(p, "fp8")
+    with pytest.raises(ValueError):
+        flash_attn_func(q, k, v, p_mode="noblock")
 
 
 def test_descales_per_batch_and_kv_head():
