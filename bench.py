@@ -59,7 +59,8 @@ def parse():
                     help="measure the dense FP8 and BF16 tcgen05 MMA rate (burst and sustained) instead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--host-chunks", type=int, default=0,
-                    help="chunks of the host-buffer call in the e2e leg (0 = the library default, 4)")
+                    help="chunks of the host-buffer call in the e2e leg (0 = the library's plan: six chunks, four "
+                         "equal ones and two short tails, from 32 query blocks of 256 rows; else four)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
     return ap.parse_args()
@@ -72,6 +73,14 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def library_host_chunks(S):
+    """Chunks the host-buffer entry point uses for chunks = 0 (its documented plan): from 32 query
+    blocks of 256 rows, four equal chunks and two short tails; below that, four equal chunks (at most
+    one per block)."""
+    nqb = (S + 255) // 256
+    return 6 if nqb >= 32 else min(4, nqb)
 
 
 def kernel_source_hash():
@@ -681,7 +690,8 @@ def main():
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": te,
                "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
                "steps": n_e2e, "call": "zyfa_attn_fwd_causal_host (pinned host buffers)",
-               "chunks": args.host_chunks or 4}
+               "chunks": args.host_chunks or library_host_chunks(sh.S),
+               "plan": "given" if args.host_chunks else "library default"}
 
     far_fraction = None
     if rank == 0 and sh.kind == "mistral" and p.q is not None:
