@@ -618,6 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait_warp(smem_u32(&ctl.s_free), s_seq & 1, abort_flag, kWaitLimit))) break;
             tc_fence_after();
             issue_s(1, st);
+            // query tile 1 normally has one more K/V tile than tile 0 and ends after this block; a
+            // unit whose two tiles end together ends tile 1 here
+            if (j == n1 - 1) tc_commit(smem_u32(&ctl.q_empty[1]));
             if (C::kSplitKV) tc_commit(smem_u32(&ctl.k_empty[st]));  // S1(j): last reader of K tile j
             const uint32_t st1 = (kv_cnt + j - 1) % C::kStages;
             if constexpr (C::kSplitKV) {

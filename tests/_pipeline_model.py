@@ -40,14 +40,21 @@ class Barrier:
 
 
 def tiles_for(S, BN, r0, t):
-    first = r0 + t * ROWS
+    """K/V tiles of query tile t of a unit.  A unit is either an int r0 (rows [r0, r0 + 256) of one
+    head: tile t starts at r0 + 128 t) or a pair (r0, r0) (the same 128 rows of two heads that share
+    a KV head: both tiles start at r0)."""
+    first = r0[t] if isinstance(r0, tuple) else r0 + t * ROWS
     if first >= S:
         return 0
     return (min(first + ROWS, S) + BN - 1) // BN
 
 
-def simulate(S, BN, stages, units, seed, wrong_release=False, max_steps=2_000_000):
-    """Run one random schedule; returns the list of protocol violations (empty when clean)."""
+def simulate(S, BN, stages, units, seed, wrong_release=False, steady_without_q1_release=False,
+             max_steps=2_000_000):
+    """Run one random schedule; returns the list of protocol violations (empty when clean).
+
+    wrong_release and steady_without_q1_release plant a mistake (in the K/V release rule, or a
+    steady block that never releases query tile 1's Q buffer) that the checks must catch."""
     rnd = random.Random(seed)
     split = stages <= 3
     bars = {}
@@ -156,6 +163,21 @@ def simulate(S, BN, stages, units, seed, wrong_release=False, max_steps=2_000_00
             if (t == 0) == pv0_last:
                 pipe.append(("commit", f"v_empty{st}" if split else f"k_empty{st}"))
 
+        def issue_s(t, j, st, r0, n, q1_release=True):
+            # one score MMA and its commits, as the steady block issues it
+            nonlocal s_seq
+            if k_data[st] != (r0, j) or q_data[t] != r0:
+                errors.append(f"S{t}({j}) of unit {r0} reads K of {k_data[st]}, Q of {q_data[t]}")
+            k_refs[st] += 1
+            q_refs[t] += 1
+            pipe.append(("s", t, j, st, r0))
+            pipe.append(("commit", f"s_full{t}"))
+            if split and (t == 1 or j >= n[1]):
+                pipe.append(("commit", f"k_empty{st}"))
+            s_seq += 1
+            if j == n[t] - 1 and (t == 0 or q1_release):
+                pipe.append(("commit", f"q_empty{t}"))
+
         def issue_tail():
             n0, n1, kvb, r0 = tail
             for t, nt in ((0, n0), (1, n1)):
@@ -171,6 +193,20 @@ def simulate(S, BN, stages, units, seed, wrong_release=False, max_steps=2_000_00
                     yield wait(f"q_full{t}", q_cnt[t])
                     q_cnt[t] += 1
             for j in range(max(n)):
+                if j >= 1 and j < n[0] and n[1] > 0:
+                    # steady state (both query tiles active), the kernel's branch-free block:
+                    # S0(j), PV1(j-2), S1(j), PV0(j-1); each score MMA after the read of the previous one
+                    st = (kv_cnt + j) % stages
+                    yield wait(f"k_full{st}", (kv_cnt + j) // stages)
+                    yield wait("s_free", s_seq - 1)
+                    issue_s(0, j, st, r0, n)
+                    if j >= 2:
+                        yield from do_pv(1, j - 2, kv_cnt, n[0], n[1], r0)
+                    yield wait("s_free", s_seq - 1)
+                    issue_s(1, j, st, r0, n, q1_release=not steady_without_q1_release)
+                    yield from do_pv(0, j - 1, kv_cnt, n[0], n[1], r0)
+                    read_pending, last = True, (1, j)
+                    continue
                 for t in range(2):
                     if j >= n[t]:
                         continue
