@@ -34,3 +34,15 @@ def test_reference_arm_prints_one_line_in_the_bench_format():
 def test_reference_arm_other_ranks_do_no_work():
     r = _run({"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_e2e_record_names_the_library_chunk_plan():
+    # the host-buffer entry point's plan for chunks = 0 (include/zyfa.h): from 32 query blocks of 256
+    # rows, four equal chunks and two short tails; below that four equal chunks, at most one per block
+    import bench
+    assert bench.library_host_chunks(32768) == 6
+    assert bench.library_host_chunks(32 * 256) == 6
+    assert bench.library_host_chunks(31 * 256) == 4
+    assert bench.library_host_chunks(4096) == 4
+    assert bench.library_host_chunks(600) == 3
+    assert bench.library_host_chunks(1) == 1
