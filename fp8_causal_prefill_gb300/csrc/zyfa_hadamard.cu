@@ -61,6 +61,11 @@ __device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 // One N-wide Hadamard block held by one thread, transformed in place: stages h = 1, 2, 4, ...,
 // butterflies (a + b, a - b), then one multiply by fl32(1/sqrt(N)).  From h = 2 on, the butterflies
@@ -85,8 +90,9 @@ __device__ __forceinline__ void fwht(float (&v)[N]) {
     }
   }
   const float c = N == 128 ? 0.088388347648318440550f : 0.125f;  // fl32(1/sqrt(N))
+  const uint64_t c2 = pk(c, c);
 #pragma unroll
-  for (int i = 0; i < N; ++i) v[i] = __fmul_rn(v[i], c);
+  for (int i = 0; i < N; i += 2) upk(mul2(pk(v[i], v[i + 1]), c2), v[i], v[i + 1]);
 }
 
 // A thread's row slot in shared memory: the row's D bf16 values, padded by 16 bytes so that the
@@ -242,6 +248,7 @@ __global__ void __launch_bounds__(kThreads) hadamard_quant_kernel(const __grid_c
     const long long r = r0 + threadIdx.x;
     const long long rows = t.rows[kc];
     const float scale = kc ? sc[1] : sc[0];
+    const uint64_t scale2 = pk(scale, scale);
     __syncwarp();  // every lane has read the slots the next copies overwrite
     long long rn;
     const int kn = block_tensor(t, pb + gridDim.x, rn);
@@ -262,8 +269,10 @@ __global__ void __launch_bounds__(kThreads) hadamard_quant_kernel(const __grid_c
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const float* e = v + 16 * i + 4 * q;
-            w[q] = cvt_e4m3x2(__fmul_rn(e[1], scale), __fmul_rn(e[0], scale)) |
-                   (cvt_e4m3x2(__fmul_rn(e[3], scale), __fmul_rn(e[2], scale)) << 16);
+            float y0, y1, y2, y3;
+            upk(mul2(pk(e[0], e[1]), scale2), y0, y1);
+            upk(mul2(pk(e[2], e[3]), scale2), y2, y3);
+            w[q] = cvt_e4m3x2(y1, y0) | (cvt_e4m3x2(y3, y2) << 16);
           }
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + c * N + 16 * i), "r"(w[0]),
                        "r"(w[1]), "r"(w[2]), "r"(w[3])
