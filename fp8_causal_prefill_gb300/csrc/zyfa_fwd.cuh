@@ -65,7 +65,14 @@ constexpr int kRegsLaunch = 168;
 constexpr int kRegsControl = 72;
 constexpr int kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
-constexpr int kRescaleBinades = 8;   // lazy reference update threshold (binades)
+// Lazy reference: a row's reference exponent moves (and O and l are rescaled by the exact power of two)
+// only when a tile's largest block exponent exceeds it by more than this many binades.  Where the
+// probabilities themselves are formed against the reference (BF16, and FP8 without block scaling) it
+// must keep them inside the format: 8 binades.  With per-block scaling the codes are formed against
+// their own block and the scale factors carry the difference: 2^(e - M) up to 2^64 keeps the scale
+// factors inside e8m0 and O below 448 * 448 * 2^64 per key, far inside fp32 for any sequence length.
+constexpr int kRescaleBinades = 8;
+constexpr int kRescaleBinadesScaled = 64;
 constexpr float kLeanPC0 = 55.625f;  // Lean-P constant: code(2^x) = rne(8x + 55.625)
 constexpr long long kWaitLimit = 1ll << 31;  // ~1 s of SM clocks before a wait gives up
 constexpr int kNoExp = -2147483647;  // block exponent of a fully masked block
@@ -769,6 +776,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float a8 = a * 0.125f;     // exact: binade units for the exact-P exponential
 
       int m_ref = 0;
+      const int rescale_binades =
+          FP8 && !(EXACT && p.no_block_scale) ? kRescaleBinadesScaled : kRescaleBinades;
       float l_bf16 = 0.0f;  // BF16: fp32 sum of the rounded probabilities of this row
       // Iteration j copies score tile j out of the shared S buffer and releases it (the release also
       // tells the MMA warp that P of tile j-1, stored before, is in place), computes P of tile j and
@@ -812,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           else e[b] = empty ? kNoExp : static_cast<int>(ceilf(__fmul_rn(mx, a)));
           e_top = max(e_top, e[b]);
         }
-        const bool need = j > 0 && e_top > m_ref + kRescaleBinades;
+        const bool need = j > 0 && e_top > m_ref + rescale_binades;
         const float f = need ? exp2i(m_ref - e_top) : 1.0f;
         if (j == 0 || need) m_ref = e_top;
 
