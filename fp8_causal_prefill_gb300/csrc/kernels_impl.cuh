@@ -51,6 +51,7 @@ cudaError_t launch_fwd(const LaunchArgs& a) {
   p.lse = a.lse;
   p.desc_per_head = a.desc_per_head;
   p.no_block_scale = a.no_block_scale;
+  p.rescale_binades = a.rescale_binades;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(kThreads);

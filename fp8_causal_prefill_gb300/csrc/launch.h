@@ -25,6 +25,7 @@ struct LaunchArgs {
   float* lse;         // optional log-sum-exp output [B,H,S]
   int desc_per_head;  // descales indexed by (batch, KV head)
   int no_block_scale; // exact P only: round against the row reference, no per-block scaling
+  int rescale_binades;  // block-scaled FP8: largest lag of the row reference before a rescale
   int grid;
   Maps maps;
   cudaStream_t stream;

@@ -218,6 +218,11 @@ zyfa_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, i
   a.lse = o.lse;
   a.desc_per_head = fp8 ? o.descale_per_kv_head : 0;
   a.no_block_scale = fp8 && o.p_mode == ZYFA_P_EXACT_NO_BLOCK_SCALE ? 1 : 0;
+  // Block-scaled FP8: a block's largest weight is at most 1 and |v| at most 448, so with the row
+  // reference lagging the row's largest block exponent by at most L binades each key adds at most
+  // 448 * 2^L to O (and 2^L to l): over S keys below 2^(8.8 + L + log2 S), which fp32 holds while
+  // L + log2 S < 118.  96 binades up to 2^21 keys, 64 beyond; the e8m0 scale factors hold either.
+  a.rescale_binades = S <= (1 << 21) ? 96 : 64;
   if (fp8 && (o.p_mode == ZYFA_P_EXACT || o.p_mode == ZYFA_P_EXACT_NO_BLOCK_SCALE)) {
     if (D_qk == 64) return run<true, 64, 64, true>(a, q, k, v);
     if (D_qk == 128) return run<true, 128, 128, true>(a, q, k, v);

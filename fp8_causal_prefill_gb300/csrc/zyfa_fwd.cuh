@@ -66,13 +66,12 @@ constexpr int kRegsControl = 72;
 constexpr int kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 // Lazy reference: a row's reference exponent moves (and O and l are rescaled by the exact power of two)
-// only when a tile's largest block exponent exceeds it by more than this many binades.  Where the
+// only when a tile's largest block exponent exceeds it by more than p.rescale_binades.  Where the
 // probabilities themselves are formed against the reference (BF16, and FP8 without block scaling) it
 // must keep them inside the format: 8 binades.  With per-block scaling the codes are formed against
-// their own block and the scale factors carry the difference: 2^(e - M) up to 2^64 keeps the scale
-// factors inside e8m0 and O below 448 * 448 * 2^64 per key, far inside fp32 for any sequence length.
+// their own block (largest weight at most 1) and the scale factors carry the difference, so the host
+// allows the widest lag the fp32 accumulators bear for the launch's sequence length (see zyfa_api.cu).
 constexpr int kRescaleBinades = 8;
-constexpr int kRescaleBinadesScaled = 64;
 constexpr float kLeanPC0 = 55.625f;  // Lean-P constant: code(2^x) = rne(8x + 55.625)
 constexpr long long kWaitLimit = 1ll << 31;  // ~1 s of SM clocks before a wait gives up
 constexpr int kNoExp = -2147483647;  // block exponent of a fully masked block
@@ -156,6 +155,7 @@ struct Params {
   float* lse;       // optional [B,H,S] natural-log sum of exp of the scores (nullptr: not written)
   int desc_per_head;  // descales are arrays [B][H_kv] (1) or single values (0)
   int no_block_scale; // exact P only: every block rounds against the row reference (scale factor 1)
+  int rescale_binades;  // block-scaled FP8: lag of the row reference before O and l are rescaled
 };
 
 struct __align__(8) SharedCtl {
@@ -777,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       int m_ref = 0;
       const int rescale_binades =
-          FP8 && !(EXACT && p.no_block_scale) ? kRescaleBinadesScaled : kRescaleBinades;
+          FP8 && !(EXACT && p.no_block_scale) ? p.rescale_binades : kRescaleBinades;
       float l_bf16 = 0.0f;  // BF16: fp32 sum of the rounded probabilities of this row
       // Iteration j copies score tile j out of the shared S buffer and releases it (the release also
       // tells the MMA warp that P of tile j-1, stored before, is in place), computes P of tile j and
