@@ -1,6 +1,8 @@
-"""Edge cases at the extremes: a sequence four times the bench length, and score ranges so wide that
+"""Edge cases at the extremes: a sequence four times the bench length; score ranges so wide that
 whole 64-key blocks fall more than 127 binades below the row's reference (their E8M0 scale leaves the
-representable range; the method's weights there are below 2^-127 of the row's largest and vanish)."""
+representable range; the method's weights there are below 2^-127 of the row's largest and vanish); and
+scores that climb ~90 binades along a row, which the block-scaled paths absorb without moving the
+row's reference."""
 import numpy as np
 import pytest
 import torch
@@ -62,3 +64,35 @@ def test_extreme_score_range_bf16():
     got = select(out)
     assert np.all(np.isfinite(got))
     assert O.rel_l2(got, oracle_out(p, "bf16")) <= BF16_TOL
+
+
+@pytest.mark.parametrize("p_mode", ["lean", "exact"])
+def test_row_reference_lagging_by_up_to_ninety_binades(p_mode):
+    # Scores that rise along the keys: q = e_0 (and 0.5 e_0 for the second head), k_j = r_j e_0 with
+    # r_j climbing to 448, scaled so that a row's last keys sit ~90 binades above its first tile.  The
+    # block-scaled paths let the row reference lag that far without a rescale (the scale factors carry
+    # 2^(e - M) up to 2^90 and O grows accordingly in fp32), so the output must still match the
+    # emulation, which normalises against the row's true maximum, and stay finite.
+    S, D = 1500, 64
+    q8 = np.zeros((1, S, 2, D), dtype=np.uint8)
+    q8[:, :, 0, 0] = 0x38          # 1.0
+    q8[:, :, 1, 0] = 0x30          # 0.5
+    k8 = np.zeros((1, S, 1, D), dtype=np.uint8)
+    k8[0, :, 0, 0] = O.e4m3_encode_rne_satfinite(448.0 * np.arange(S) / (S - 1))
+    rng = np.random.default_rng(5)
+    v8 = O.e4m3_encode_rne_satfinite(rng.standard_normal((1, S, 1, D)))
+    scale, dq, dk, dv = 0.125, 1.0, 1.114, 1.0
+    a = O.fp8_score_scale(scale, dq, dk)
+    assert 700 < 448 * a < 740            # the ramp spans about 90 binades at its end
+    q, k, v = (torch.from_numpy(x).cuda().view(torch.float8_e4m3fn) for x in (q8, k8, v8))
+    ds = [torch.tensor([x], dtype=torch.float32, device="cuda") for x in (dq, dk, dv)]
+    out = flash_attn_func(q, k, v, softmax_scale=scale, q_descale=ds[0], k_descale=ds[1], v_descale=ds[2],
+                          p_mode=p_mode)
+    torch.cuda.synchronize()
+    assert zyfa_check_errors() == 0
+    f = O.exactp_causal_attention if p_mode == "exact" else O.leanp_causal_attention
+    ref = f(q8, k8, v8, dq, dk, dv, scale)
+    got = select(out)
+    assert np.all(np.isfinite(got))
+    assert O.rel_l2(got, ref) <= FP8_TOL
+    assert per_row_rel(got, ref).max() <= 5e-2
